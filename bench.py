@@ -1,0 +1,407 @@
+"""Benchmark of the PSA attention step (fused forward + dQ + dK/dV backward) on GB300.
+
+One step = psa_attention_fwd (QKV -> Out, LSE, extracted V) + psa_attention_bwd_dq
++ psa_attention_bwd_dkdv (-> dQKV) over one batch of the 'psa_fwdbwd_n400'
+workload: B=64, num_heads=4, KEY_DIM=32, 20x20 (N=400), bf16, synthetic seeded
+N(0,1) inputs.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the test oracle, untuned) on the
+host cores, on a bounded sample of the same workload per step.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the path
+has no exchange step: heads and batches are independent), so scaling is weak and
+no collective touches the data path; only the timing uses a barrier and a max.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "psa_fwdbwd_n400"
+METRIC = "PSA attention fwd+bwd tokens/s and TFLOP/s at N=400, KEY_DIM=32; % roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs") or d.get("hbm_GBps"))
+        tf = float(d.get("bf16_tflops"))
+        tfs = float(d.get("bf16_tflops_sustained", tf))
+        return {"hbm_gbs": hbm, "bf16_tflops": tf, "bf16_tflops_sustained": tfs}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- work model
+def work_model(w):
+    """Algorithmic FLOPs and HBM bytes of each kernel of one step (bf16 = 2 bytes).
+
+    fwd   : S = Q K^T (2 N^2 KD) and O = P [V_lo|V_hi] (2 N^2 2KD) per head;
+            reads QKV, writes Out, LSE and the extracted V.
+    bwd_dq: S, dP = dO V^T (2 N^2 2KD), dQ = dS K (2 N^2 KD) per head; reads QKV
+            (Q, K, V planes), Out, dOut, LSE; writes dQ and delta.
+    bwd_dkdv: S^T, dP^T, dV = P^T dO (2 N^2 2KD), dK = dS^T Q (2 N^2 KD); reads QKV,
+            dOut, LSE, delta; writes dK, dV.
+    step  : the algorithmic total (S computed once in the forward and once in the
+            backward): 192 N^2 + 448 N^2 FLOPs per head; bytes = QKV + Out + V
+            written, QKV + Out + dOut read and dQKV written, LSE written and read.
+    """
+    N, BH, KD, B = w.N, w.BH, w.key_dim, w.B
+    C, c = w.qkv_channels, w.out_channels
+    e = 2
+    n2 = float(N) * N * BH
+    lse = BH * N * 4
+    k = {
+        "fwd": {"flops": n2 * (2 * KD + 2 * 2 * KD), "bytes": B * N * (C + c + c) * e + lse},
+        "bwd_dq": {"flops": n2 * (2 * KD + 2 * 2 * KD + 2 * KD),
+                   "bytes": B * N * (C + c + c + KD * w.num_heads) * e + 2 * lse},
+        "bwd_dkdv": {"flops": n2 * (2 * KD + 2 * 2 * KD + 2 * 2 * KD + 2 * KD),
+                     "bytes": B * N * (C + c + 3 * KD * w.num_heads) * e + 2 * lse},
+    }
+    step = {"flops": n2 * (192 / 32 * KD + 448 / 32 * KD),
+            "bytes": B * N * (C + c + c) * e + lse + B * N * (C + c + c + C) * e + lse}
+    return k, step
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only) in a thread."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle"}
+
+    def __init__(self, index=0, period=0.002):
+        self.samples, self.reasons, self.ok = [], 0, False
+        self.period, self._stop = period, threading.Event()
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            pass
+
+    def _sample(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+            self.samples.append(int(c.value))
+        if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
+            self.reasons |= int(r.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._sample()
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+            self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from vision_transformer_attention_psapackqkv_gb300 import binding as B
+    from vision_transformer_attention_psapackqkv_gb300.inputs import PSA_WORKLOADS, workload_inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    w = PSA_WORKLOADS[WORKLOAD]
+    scale = 1.0 / math.sqrt(w.key_dim)
+    ins = workload_inputs(w)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    qkv0, dout0 = to_dev(ins["qkv"]), to_dev(ins["dout"])
+    shape = B.shape_of(qkv0, w.num_heads, w.key_dim)
+    # rotate input/output sets whose footprint exceeds twice the L2 (129 MB)
+    per_set = (qkv0.numel() * 2 * 2 + dout0.numel() * 2 * 3 + w.BH * w.N * 8)
+    nsets = max(3, math.ceil(2 * 2 * 129e6 / per_set))
+    sets = []
+    for i in range(nsets):
+        qkv = qkv0 if i == 0 else qkv0.roll(i, dims=0).contiguous()
+        dout = dout0 if i == 0 else dout0.roll(i, dims=0).contiguous()
+        sets.append({
+            "qkv": qkv, "dout": dout,
+            "out": torch.empty_like(dout), "vres": torch.empty_like(dout),
+            "lse": torch.empty((w.BH, w.N), dtype=torch.float32, device="cuda"),
+            "delta": torch.empty((w.BH, w.N), dtype=torch.float32, device="cuda"),
+            "dqkv": torch.empty_like(qkv),
+        })
+    stream = torch.cuda.current_stream()
+
+    def fwd(s):
+        B.psa_attention_fwd(s["qkv"], s["out"], s["lse"], s["vres"], shape, scale, stream)
+
+    def bwd_dq(s):
+        B.psa_attention_bwd_dq(s["qkv"], s["out"], s["dout"], s["lse"], s["delta"], s["dqkv"], shape,
+                               scale, stream)
+
+    def bwd_dkdv(s):
+        B.psa_attention_bwd_dkdv(s["qkv"], s["dout"], s["lse"], s["delta"], None, s["dqkv"], shape, scale,
+                                 stream)
+
+    parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
+    launches_per_step = 2 + 1 + 1  # forward attention + extract, dQ, dK/dV
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        s = sets[i % nsets]
+        for _, f in parts:
+            f(s)
+    barrier()
+    if B.psa_get_last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        start.record(stream)
+        for i in range(K):
+            s = sets[i % nsets]
+            e = ev[i]
+            e[0].record(stream)
+            fwd(s)
+            e[1].record(stream)
+            bwd_dq(s)
+            e[2].record(stream)
+            bwd_dkdv(s)
+            e[3].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    ms_total = start.elapsed_time(stop)
+    per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+           for j, (name, _) in enumerate(parts)}
+    if dist is not None:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if B.psa_get_last_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # end to end through the C ABI from pinned host buffers
+    h_qkv = sets[0]["qkv"].cpu().pin_memory()
+    h_dout = sets[0]["dout"].cpu().pin_memory()
+    h_out = torch.empty(sets[0]["out"].shape, dtype=torch.bfloat16).pin_memory()
+    h_vres = torch.empty_like(h_out).pin_memory()
+    h_lse = torch.empty(sets[0]["lse"].shape, dtype=torch.float32).pin_memory()
+    h_dqkv = torch.empty(sets[0]["dqkv"].shape, dtype=torch.bfloat16).pin_memory()
+    Ke = max(3, min(K, 200))
+    s = sets[0]
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        s["qkv"].copy_(h_qkv, non_blocking=True)
+        s["dout"].copy_(h_dout, non_blocking=True)
+        fwd(s)
+        bwd_dq(s)
+        bwd_dkdv(s)
+        h_out.copy_(s["out"], non_blocking=True)
+        h_vres.copy_(s["vres"], non_blocking=True)
+        h_lse.copy_(s["lse"], non_blocking=True)
+        h_dqkv.copy_(s["dqkv"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = h_qkv.numel() * 2 + h_dout.numel() * 2
+    d2h = h_out.numel() * 2 * 2 + h_lse.numel() * 4 + h_dqkv.numel() * 2
+
+    tokens_per_step = w.B * w.N
+    kmodel, step_model = work_model(w)
+    peaks, peak_src = load_peaks()
+    ms_step = ms_total / K
+    value = tokens_per_step * world * K / (ms_total / 1e3)
+    tflops = step_model["flops"] * world * K / (ms_total / 1e3) / 1e12
+    # the dominant kernel (largest time share) and its roofline
+    dom = max(per, key=per.get)
+    km = kmodel[dom]
+    t_s = per[dom] / 1e3
+    t_flop = km["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_byte = km["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_byte >= t_flop:
+        roof = {"bound": "hbm", "achieved": km["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": km["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_src
+    step_roof_time = max(step_model["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                         step_model["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) QKV and dOut)",
+        "config": {"workload": WORKLOAD, "B": w.B, "num_heads": w.num_heads, "key_dim": w.key_dim,
+                   "H": w.H, "W": w.W, "N": w.N, "global_batch": w.B * world, "seq_len": w.N,
+                   "parallelism": f"replicas x{world}", "l2": f"rotating {nsets} input/output sets "
+                   f"({nsets * per_set / 1e6:.0f} MB > 2 x L2)"},
+        "tflops": tflops,
+        "step_roofline": {"frac": step_roof_time / (ms_step / 1e3), "roofline_us": step_roof_time * 1e6,
+                          "flops": step_model["flops"], "bytes": step_model["bytes"],
+                          "peak_source": peak_src},
+        "kernel_us": {k: v * 1e3 for k, v in per.items()},
+        "roofline": roof,
+        "e2e": {"value": tokens_per_step * world * Ke / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, scale, budget_s=args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------------------- the oracle on CPU
+def cpu_baseline(w, scale, budget_s=15.0, batches=None):
+    """Times the fp64 oracle (PSA forward + backward) on the first `batches` batch
+    items of the workload's inputs, on all host cores."""
+    import oracle
+    from vision_transformer_attention_psapackqkv_gb300.inputs import storage_to_f64, workload_inputs
+
+    oracle.build()
+    ins = workload_inputs(w)
+    threads = oracle.default_threads()
+
+    def run(nb):
+        q = storage_to_f64(ins["qkv"][:nb], w.dtype)
+        d = storage_to_f64(ins["dout"][:nb], w.dtype)
+        t0 = time.perf_counter()
+        oracle.psa_fwd(q, w.num_heads, w.key_dim, scale, nthreads=threads)
+        oracle.psa_bwd(q, d, w.num_heads, w.key_dim, scale, nthreads=threads)
+        return time.perf_counter() - t0
+
+    if batches is None:
+        nb = max(1, math.ceil(threads / w.num_heads))
+        t = run(nb)
+        while t < budget_s / 4 and nb < w.B:
+            nb = min(w.B, nb * 2)
+            t = run(nb)
+    else:
+        nb = batches
+        t = run(nb)
+    return {"value": nb * w.N / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nb} of {w.B} batch items ({nb * w.num_heads} heads, {nb * w.N} tokens), "
+                      f"fp64 forward + backward, {t:.2f} s"}
+
+
+def run_reference(args):
+    from vision_transformer_attention_psapackqkv_gb300.inputs import PSA_WORKLOADS
+
+    w = PSA_WORKLOADS[WORKLOAD]
+    scale = 1.0 / math.sqrt(w.key_dim)
+    import oracle
+    from vision_transformer_attention_psapackqkv_gb300.inputs import storage_to_f64, workload_inputs
+
+    oracle.build()
+    ins = workload_inputs(w)
+    threads = oracle.default_threads()
+    nb = 2  # batch items per step: 8 heads, 800 tokens
+    q = storage_to_f64(ins["qkv"][:nb], w.dtype)
+    d = storage_to_f64(ins["dout"][:nb], w.dtype)
+
+    def step():
+        oracle.psa_fwd(q, w.num_heads, w.key_dim, scale, nthreads=threads)
+        oracle.psa_bwd(q, d, w.num_heads, w.key_dim, scale, nthreads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    value = nb * w.N * args.steps / t
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) QKV and dOut)",
+        "config": {"workload": WORKLOAD, "B": w.B, "num_heads": w.num_heads, "key_dim": w.key_dim,
+                   "H": w.H, "W": w.W, "N": w.N, "step_sample_batches": nb},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{nb} of {w.B} batch items per step ({nb * w.num_heads} heads)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

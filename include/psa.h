@@ -1,0 +1,172 @@
+/*
+ * psa.h -- C ABI of the GB300 (sm_103a) Position-Sensitive Attention library
+ * (libpsa_gb300.so).
+ *
+ * The operations are those of the vision-rs book, page "Custom Kernels":
+ *   section "Flash Attention 2"  -- softmax attention over [BATCH*N_HEADS, N_CTX,
+ *     HEAD_DIM] tensors with an online softmax (the N x N matrix is never stored);
+ *     the forward, the dQ backward and the dK/dV backward are separate kernels.
+ *   section "Position-Sensitive Attention (PSA)" -- PsaPackQkv, PsaExtractV and
+ *     PsaMergeAttn around Flash Attention 2, which PSA runs once per V half
+ *     (V_lo, V_hi) with HEAD_DIM = KEY_DIM.
+ *
+ * Notation: KD = key_dim, nh = num_heads, N = H*W, BH = B*nh, qkv_h = nh*4*KD,
+ * c = nh*2*KD.  Spatial index n = h*W + w; head-batch index bh = b*nh + head.
+ * Per head, QKV channels are [Q | K | V_lo | V_hi], each KD wide: channel
+ * head*4*KD + s*KD + d holds element d of plane s (0=Q, 1=K, 2=V_lo, 3=V_hi).
+ * The merged output channel head*2*KD + t*KD + d holds element d of half t.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers to dense, contiguous buffers owned
+ *     by the caller; the library never allocates, frees or synchronises, and
+ *     every call is ordered on the given stream.  Pointers must be 16-byte
+ *     aligned (PSA_ERR_ALIGNMENT otherwise).
+ *   - Arguments come in the order inputs, outputs, workspace, sizes, stream.
+ *   - Validation is host-side and happens before any launch: a NULL required
+ *     pointer or a non-positive size gives PSA_ERR_INVALID_ARG; a size the
+ *     kernels do not implement gives PSA_ERR_UNSUPPORTED; a failed launch gives
+ *     PSA_ERR_CUDA.  Nothing is printed and nothing exits.
+ *   - Element types: bf16 (PSA_DTYPE_BF16; fp32 accumulation, softmax
+ *     probabilities rounded to bf16 before the P.V product, outputs rounded to
+ *     nearest-even) or fp32 (PSA_DTYPE_F32; forward only, fp32 arithmetic).
+ *     Log-sum-exp and delta arrays are always fp32.
+ *   - Kernels that wait on on-chip barriers give up after a bounded time and
+ *     record PSA_ERR_TIMEOUT in a device-side error word that
+ *     psa_get_last_device_error() reads and clears.
+ */
+#ifndef PSA_GB300_H
+#define PSA_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PSA_OK = 0,
+    PSA_ERR_INVALID_ARG = 1,
+    PSA_ERR_UNSUPPORTED = 2,
+    PSA_ERR_ALIGNMENT = 3,
+    PSA_ERR_CUDA = 4,
+    PSA_ERR_TIMEOUT = 5
+} psa_status_t;
+
+typedef enum { PSA_DTYPE_F32 = 0, PSA_DTYPE_BF16 = 1 } psa_dtype_t;
+
+/* One PSA problem: QKV conv output [B, nh*4*KD, H, W] of the given element type. */
+typedef struct {
+    int B, num_heads, key_dim, H, W;
+    psa_dtype_t dtype;
+} psa_shape_t;
+
+/* ---- layout kernels (bit-exact element copies) ------------------------------ */
+
+/* PsaPackQkv ("Custom Kernels", section "Position-Sensitive Attention (PSA)"):
+ * qkv_nchw [B, qkv_h, H, W] -> packed [4, BH, N, KD] (planes Q, K, V_lo, V_hi).
+ * Both dtypes; key_dim up to 128 for all layout kernels. */
+psa_status_t psa_pack_qkv(const void *qkv_nchw, void *packed, psa_shape_t shape,
+                          cudaStream_t stream);
+
+/* Inverse permutation of psa_pack_qkv (the adjoint the backward needs):
+ * packed [4, BH, N, KD] -> qkv_nchw [B, qkv_h, H, W]. */
+psa_status_t psa_unpack_qkv(const void *packed, void *qkv_nchw, psa_shape_t shape,
+                            cudaStream_t stream);
+
+/* PsaExtractV (same section): the V section [V_lo | V_hi] of every head, as NCHW
+ * v_nchw [B, c, H, W] (v_nchw[b, head*2KD + j, n] = qkv[b, head*4KD + 2KD + j, n]). */
+psa_status_t psa_extract_v(const void *qkv_nchw, void *v_nchw, psa_shape_t shape,
+                           cudaStream_t stream);
+
+/* PsaMergeAttn (same section): o_lo, o_hi [BH, N, KD] -> out_nchw [B, c, H, W]. */
+psa_status_t psa_merge_attn(const void *o_lo, const void *o_hi, void *out_nchw,
+                            psa_shape_t shape, cudaStream_t stream);
+
+/* Inverse of psa_merge_attn (the adjoint the backward needs):
+ * dout_nchw [B, c, H, W] -> do_lo, do_hi [BH, N, KD]. */
+psa_status_t psa_unmerge_attn(const void *dout_nchw, void *do_lo, void *do_hi,
+                              psa_shape_t shape, cudaStream_t stream);
+
+/* ---- Flash Attention 2 on [BH, N, HEAD_DIM] ("Flash Attention 2" section) ---- */
+
+/* Forward: o = softmax(scale * q k^T) v, lse = log-sum-exp of each score row
+ * (natural log, fp32 [BH, n_ctx]; lse may be NULL).  q, k, v, o are
+ * [BH, n_ctx, head_dim] of dtype; head_dim in {32, 64} (PSA_ERR_UNSUPPORTED
+ * otherwise).  Non-causal, no mask. */
+psa_status_t flash_attn2_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int BH, int n_ctx, int head_dim, float scale, psa_dtype_t dtype,
+                             cudaStream_t stream);
+
+/* dQ backward: writes delta[bh, i] = sum_c do[bh, i, c] * o[bh, i, c] (fp32
+ * [BH, n_ctx], caller-owned) and dq = scale * dS k with dS = P o (dP - delta),
+ * P = exp(scale q k^T - lse), dP = do v^T.  lse is the forward's.  bf16 only.
+ * Must run before flash_attn2_bwd_dkdv, which reads delta. */
+psa_status_t flash_attn2_bwd_dq(const void *q, const void *k, const void *v, const void *o,
+                                const void *do_, const float *lse, float *delta, void *dq,
+                                int BH, int n_ctx, int head_dim, float scale, psa_dtype_t dtype,
+                                cudaStream_t stream);
+
+/* dK/dV backward: dv = P^T do, dk = scale * dS^T q, with delta from
+ * flash_attn2_bwd_dq.  bf16 only.  dk, dv are overwritten. */
+psa_status_t flash_attn2_bwd_dkdv(const void *q, const void *k, const void *v, const void *do_,
+                                  const float *lse, const float *delta, void *dk, void *dv,
+                                  int BH, int n_ctx, int head_dim, float scale,
+                                  psa_dtype_t dtype, cudaStream_t stream);
+
+/* ---- fused PSA reading and writing NCHW directly ----------------------------- */
+
+/* Forward of the whole PSA attention step: pack, attention over both V halves
+ * with one shared softmax (identical to two HEAD_DIM = KD runs), merge; writes
+ * out_nchw [B, c, H, W], lse [BH, N] fp32 (nullable) and, when v_nchw is not
+ * NULL, the PsaExtractV output [B, c, H, W].  key_dim in {32, 64};
+ * N*sizeof(dtype) must be a multiple of 16 (PSA_ERR_ALIGNMENT otherwise);
+ * bf16, or fp32 (computed in fp32). */
+psa_status_t psa_attention_fwd(const void *qkv_nchw, void *out_nchw, float *lse, void *v_nchw,
+                               psa_shape_t shape, float scale, cudaStream_t stream);
+
+/* Backward of psa_attention_fwd: given qkv, the forward's out and lse, the
+ * upstream gradient dout [B, c, H, W] and optionally the gradient dvres of the
+ * extracted V (nullable), writes dqkv_nchw [B, qkv_h, H, W] (overwritten, V
+ * channels include dvres).  workspace must hold
+ * psa_attention_bwd_workspace_size(shape) bytes (device, 16-byte aligned).
+ * bf16 only; key_dim 32 or 64. */
+psa_status_t psa_attention_bwd(const void *qkv_nchw, const void *out_nchw, const void *dout_nchw,
+                               const float *lse, const void *dvres_nchw, void *dqkv_nchw,
+                               void *workspace, size_t ws_bytes, psa_shape_t shape, float scale,
+                               cudaStream_t stream);
+
+/* The two kernels psa_attention_bwd runs, for callers that schedule them
+ * separately ("Flash Attention 2" section: the dQ and dK/dV backward are separate
+ * kernels with their own grids).  psa_attention_bwd_dq writes the Q channels of
+ * dqkv_nchw and delta [BH, N] fp32 (rowsum of dOut o Out per head and position);
+ * psa_attention_bwd_dkdv then reads delta and writes the K and V channels (V
+ * channels include dvres when it is not NULL).  It must run after
+ * psa_attention_bwd_dq on the same stream.  Same sizes and errors as
+ * psa_attention_bwd. */
+psa_status_t psa_attention_bwd_dq(const void *qkv_nchw, const void *out_nchw,
+                                  const void *dout_nchw, const float *lse, float *delta,
+                                  void *dqkv_nchw, psa_shape_t shape, float scale,
+                                  cudaStream_t stream);
+psa_status_t psa_attention_bwd_dkdv(const void *qkv_nchw, const void *dout_nchw,
+                                    const float *lse, const float *delta,
+                                    const void *dvres_nchw, void *dqkv_nchw, psa_shape_t shape,
+                                    float scale, cudaStream_t stream);
+
+/* Bytes of device workspace psa_attention_bwd needs (0 for an invalid shape). */
+size_t psa_attention_bwd_workspace_size(psa_shape_t shape);
+
+/* ---- status ------------------------------------------------------------------- */
+
+/* Static description of a status code. */
+const char *psa_status_string(psa_status_t status);
+
+/* Synchronises the stream, then reads and clears the device-side error word
+ * (PSA_ERR_TIMEOUT after a bounded on-chip wait gave up; PSA_OK otherwise). */
+psa_status_t psa_get_last_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSA_GB300_H */

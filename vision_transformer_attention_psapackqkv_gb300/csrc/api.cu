@@ -1,0 +1,387 @@
+// api.cu -- the C ABI of include/psa.h: host-side validation, TMA tensor maps and
+// launches.  No entry point allocates, frees or synchronises (except
+// psa_get_last_device_error, which is documented to synchronise).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/psa.h"
+#include "attn.cuh"
+#include "layout.cuh"
+
+namespace psa {
+__device__ int g_device_error = 0;
+}
+
+namespace {
+
+using psa::BwdArgs;
+using psa::FwdArgs;
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(psa_dtype_t t) { return t == PSA_DTYPE_F32 ? 4 : 2; }
+
+psa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? PSA_OK : PSA_ERR_CUDA; }
+
+psa_status_t check_shape(const psa_shape_t& s) {
+  if (s.B <= 0 || s.num_heads <= 0 || s.key_dim <= 0 || s.H <= 0 || s.W <= 0)
+    return PSA_ERR_INVALID_ARG;
+  if (s.dtype != PSA_DTYPE_F32 && s.dtype != PSA_DTYPE_BF16) return PSA_ERR_INVALID_ARG;
+  if (s.key_dim > 128) return PSA_ERR_UNSUPPORTED;  // layout tiles stage KD x 64 in shared memory
+  // every index of the largest tensor must fit the kernels' int coordinates
+  const long long n = (long long)s.H * s.W;
+  const long long big = (long long)s.B * s.num_heads * 4 * s.key_dim * n;
+  if (n > (1LL << 30) || big > (1LL << 40) || (long long)s.B * s.num_heads * 4 * s.key_dim > (1LL << 30))
+    return PSA_ERR_UNSUPPORTED;
+  return PSA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time
+// dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(uint32_t inner_bytes) {
+  return inner_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+}
+
+// 3-D bf16 map over [BH, N, d] (d contiguous), box {d, box_rows, 1}.
+bool map_rows(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows = 128) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(d * 2),
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 map over an NCHW tensor viewed as [rows, N] (N contiguous), box {64, box_rows}.
+bool map_nchw(CUtensorMap* m, const void* base, long long rows, int N, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+psa_status_t check_fa2(const void* const* ptrs, int nptr, int BH, int n_ctx, int head_dim,
+                       float scale, psa_dtype_t dtype) {
+  for (int i = 0; i < nptr; ++i) {
+    if (!ptrs[i]) return PSA_ERR_INVALID_ARG;
+    if (!aligned16(ptrs[i])) return PSA_ERR_ALIGNMENT;
+  }
+  if (BH <= 0 || n_ctx <= 0 || head_dim <= 0 || !isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (dtype != PSA_DTYPE_F32 && dtype != PSA_DTYPE_BF16) return PSA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64) return PSA_ERR_UNSUPPORTED;
+  if ((long long)BH > 65535 || (long long)n_ctx > (1LL << 28)) return PSA_ERR_UNSUPPORTED;
+  return PSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psa_status_string(psa_status_t s) {
+  switch (s) {
+    case PSA_OK: return "PSA_OK";
+    case PSA_ERR_INVALID_ARG: return "PSA_ERR_INVALID_ARG: null pointer, non-positive size or bad enum";
+    case PSA_ERR_UNSUPPORTED: return "PSA_ERR_UNSUPPORTED: size or dtype not implemented";
+    case PSA_ERR_ALIGNMENT: return "PSA_ERR_ALIGNMENT: pointer or row not 16-byte aligned";
+    case PSA_ERR_CUDA: return "PSA_ERR_CUDA: a CUDA call or launch failed";
+    case PSA_ERR_TIMEOUT: return "PSA_ERR_TIMEOUT: an on-chip wait gave up";
+  }
+  return "unknown psa_status_t";
+}
+
+psa_status_t psa_get_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, psa::g_device_error, sizeof(int)) != cudaSuccess) return PSA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(psa::g_device_error, &zero, sizeof(int)) != cudaSuccess) return PSA_ERR_CUDA;
+  }
+  return v == 0 ? PSA_OK : (psa_status_t)v;
+}
+
+// ---------------------------------------------------------------- layout entry points
+psa_status_t psa_pack_qkv(const void* qkv, void* packed, psa_shape_t s, cudaStream_t st) {
+  if (!qkv || !packed) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!aligned16(qkv) || !aligned16(packed)) return PSA_ERR_ALIGNMENT;
+  return from_cuda(psa::launch_pack_qkv(qkv, packed, s.B, s.num_heads, s.key_dim, s.H * s.W,
+                                        elem_bytes(s.dtype), st));
+}
+
+psa_status_t psa_unpack_qkv(const void* packed, void* qkv, psa_shape_t s, cudaStream_t st) {
+  if (!qkv || !packed) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!aligned16(qkv) || !aligned16(packed)) return PSA_ERR_ALIGNMENT;
+  return from_cuda(psa::launch_unpack_qkv(packed, qkv, s.B, s.num_heads, s.key_dim, s.H * s.W,
+                                          elem_bytes(s.dtype), st));
+}
+
+psa_status_t psa_extract_v(const void* qkv, void* v, psa_shape_t s, cudaStream_t st) {
+  if (!qkv || !v) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!aligned16(qkv) || !aligned16(v)) return PSA_ERR_ALIGNMENT;
+  if ((2LL * s.key_dim * s.H * s.W * elem_bytes(s.dtype)) % 16 != 0) return PSA_ERR_ALIGNMENT;
+  return from_cuda(psa::launch_extract_v(qkv, v, s.B, s.num_heads, s.key_dim, s.H * s.W,
+                                         elem_bytes(s.dtype), st));
+}
+
+psa_status_t psa_merge_attn(const void* o_lo, const void* o_hi, void* out, psa_shape_t s,
+                            cudaStream_t st) {
+  if (!o_lo || !o_hi || !out) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!aligned16(o_lo) || !aligned16(o_hi) || !aligned16(out)) return PSA_ERR_ALIGNMENT;
+  return from_cuda(psa::launch_merge_attn(o_lo, o_hi, out, s.B, s.num_heads, s.key_dim,
+                                          s.H * s.W, elem_bytes(s.dtype), st));
+}
+
+psa_status_t psa_unmerge_attn(const void* dout, void* do_lo, void* do_hi, psa_shape_t s,
+                              cudaStream_t st) {
+  if (!dout || !do_lo || !do_hi) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!aligned16(dout) || !aligned16(do_lo) || !aligned16(do_hi)) return PSA_ERR_ALIGNMENT;
+  return from_cuda(psa::launch_unmerge_attn(dout, do_lo, do_hi, s.B, s.num_heads, s.key_dim,
+                                            s.H * s.W, elem_bytes(s.dtype), st));
+}
+
+// ---------------------------------------------------------------- Flash Attention 2
+psa_status_t flash_attn2_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int BH, int n_ctx, int head_dim, float scale, psa_dtype_t dtype,
+                             cudaStream_t st) {
+  const void* ptrs[4] = {q, k, v, o};
+  psa_status_t e = check_fa2(ptrs, 4, BH, n_ctx, head_dim, scale, dtype);
+  if (e != PSA_OK) return e;
+  if (lse && !aligned16(lse)) return PSA_ERR_ALIGNMENT;
+  if (dtype == PSA_DTYPE_F32)
+    return from_cuda(psa::launch_fa2_fwd_f32((const float*)q, (const float*)k, (const float*)v,
+                                             (float*)o, lse, BH, n_ctx, head_dim, scale, st));
+  CUtensorMap mq, mk, mv;
+  if (!map_rows(&mq, q, BH, n_ctx, head_dim) || !map_rows(&mk, k, BH, n_ctx, head_dim) ||
+      !map_rows(&mv, v, BH, n_ctx, head_dim))
+    return PSA_ERR_CUDA;
+  FwdArgs a{};
+  a.N = n_ctx;
+  a.nh = 1;
+  a.scale_log2 = scale * kLog2e;
+  a.out = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  return from_cuda(psa::launch_fa2_fwd_bf16(mq, mk, mv, a, BH, head_dim, st));
+}
+
+psa_status_t flash_attn2_bwd_dq(const void* q, const void* k, const void* v, const void* o,
+                                const void* do_, const float* lse, float* delta, void* dq, int BH,
+                                int n_ctx, int head_dim, float scale, psa_dtype_t dtype,
+                                cudaStream_t st) {
+  const void* ptrs[8] = {q, k, v, o, do_, lse, delta, dq};
+  psa_status_t e = check_fa2(ptrs, 8, BH, n_ctx, head_dim, scale, dtype);
+  if (e != PSA_OK) return e;
+  if (dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv, mdo;
+  // the dQ kernel walks 128-query tiles against 64-key tiles
+  if (!map_rows(&mq, q, BH, n_ctx, head_dim, 128) || !map_rows(&mk, k, BH, n_ctx, head_dim, 64) ||
+      !map_rows(&mv, v, BH, n_ctx, head_dim, 64) || !map_rows(&mdo, do_, BH, n_ctx, head_dim, 128))
+    return PSA_ERR_CUDA;
+  BwdArgs a{};
+  a.N = n_ctx;
+  a.nh = 1;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.lse = lse;
+  a.delta = delta;
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dO = static_cast<const __nv_bfloat16*>(do_);
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  return from_cuda(psa::launch_fa2_bwd_dq(mq, mk, mv, mdo, a, BH, head_dim, st));
+}
+
+psa_status_t flash_attn2_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
+                                  const float* lse, const float* delta, void* dk, void* dv,
+                                  int BH, int n_ctx, int head_dim, float scale,
+                                  psa_dtype_t dtype, cudaStream_t st) {
+  const void* ptrs[8] = {q, k, v, do_, lse, delta, dk, dv};
+  psa_status_t e = check_fa2(ptrs, 8, BH, n_ctx, head_dim, scale, dtype);
+  if (e != PSA_OK) return e;
+  if (dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv, mdo;
+  // the dK/dV kernel walks 128-key tiles against 64-query tiles
+  if (!map_rows(&mq, q, BH, n_ctx, head_dim, 64) || !map_rows(&mk, k, BH, n_ctx, head_dim, 128) ||
+      !map_rows(&mv, v, BH, n_ctx, head_dim, 128) || !map_rows(&mdo, do_, BH, n_ctx, head_dim, 64))
+    return PSA_ERR_CUDA;
+  BwdArgs a{};
+  a.N = n_ctx;
+  a.nh = 1;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.lse = lse;
+  a.delta = const_cast<float*>(delta);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  return from_cuda(psa::launch_fa2_bwd_dkdv(mq, mk, mv, mdo, a, BH, head_dim, st));
+}
+
+// ---------------------------------------------------------------- fused PSA
+psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_nchw,
+                               psa_shape_t s, float scale, cudaStream_t st) {
+  if (!qkv || !out) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
+  if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;
+  if (!aligned16(qkv) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (v_nchw && !aligned16(v_nchw)))
+    return PSA_ERR_ALIGNMENT;
+  const int N = s.H * s.W;
+  if (((long long)N * elem_bytes(s.dtype)) % 16 != 0) return PSA_ERR_ALIGNMENT;
+  const int nh = s.num_heads, KD = s.key_dim;
+  if (s.dtype == PSA_DTYPE_F32) {
+    e = from_cuda(psa::launch_psa_fwd_f32((const float*)qkv, (float*)out, lse, s.B, nh, KD, N,
+                                          scale, st));
+  } else {
+    CUtensorMap mqk, mv;
+    const long long rows = (long long)s.B * nh * 4 * KD;
+    if (!map_nchw(&mqk, qkv, rows, N, KD) || !map_nchw(&mv, qkv, rows, N, 2 * KD))
+      return PSA_ERR_CUDA;
+    FwdArgs a{};
+    a.N = N;
+    a.nh = nh;
+    a.qkv_ch = nh * 4 * KD;
+    a.out_ch = nh * 2 * KD;
+    a.scale_log2 = scale * kLog2e;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    e = from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, a, s.B * nh, KD, st));
+  }
+  if (e != PSA_OK || !v_nchw) return e;
+  return from_cuda(psa::launch_extract_v(qkv, v_nchw, s.B, nh, KD, N, elem_bytes(s.dtype), st));
+}
+
+size_t psa_attention_bwd_workspace_size(psa_shape_t s) {
+  if (check_shape(s) != PSA_OK) return 0;
+  // delta [BH, N] fp32
+  return ((size_t)s.B * s.num_heads * s.H * s.W * sizeof(float) + 255) & ~(size_t)255;
+}
+
+namespace {
+// Host-side checks shared by the fused backward entry points (no CUDA call).
+psa_status_t validate_bwd(const void* qkv, const void* dout, const float* lse, const void* dqkv,
+                          const float* delta, const void* dvres, const void* out, bool need_out,
+                          const psa_shape_t& s, float scale) {
+  if (!qkv || !dout || !lse || !dqkv || !delta || (need_out && !out)) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (!isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (s.dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
+  if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
+  if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;
+  if (!aligned16(qkv) || !aligned16(dout) || !aligned16(lse) || !aligned16(dqkv) ||
+      !aligned16(delta) || (dvres && !aligned16(dvres)) || (out && !aligned16(out)))
+    return PSA_ERR_ALIGNMENT;
+  if (((long long)s.H * s.W * 2) % 16 != 0) return PSA_ERR_ALIGNMENT;
+  return PSA_OK;
+}
+
+// Tensor maps and kernel arguments of a validated fused backward call.
+psa_status_t make_bwd(const void* qkv, const void* dout, const float* lse, const void* dqkv,
+                      const float* delta, const void* dvres, const void* out,
+                      const psa_shape_t& s, float scale, CUtensorMap* mqk, CUtensorMap* mv,
+                      CUtensorMap* mdo, BwdArgs* a) {
+  const int N = s.H * s.W;
+  const int nh = s.num_heads, KD = s.key_dim;
+  const long long rows = (long long)s.B * nh * 4 * KD;
+  if (!map_nchw(mqk, qkv, rows, N, KD) || !map_nchw(mv, qkv, rows, N, 2 * KD) ||
+      !map_nchw(mdo, dout, (long long)s.B * nh * 2 * KD, N, 2 * KD))
+    return PSA_ERR_CUDA;
+  *a = BwdArgs{};
+  a->N = N;
+  a->nh = nh;
+  a->qkv_ch = nh * 4 * KD;
+  a->out_ch = nh * 2 * KD;
+  a->scale = scale;
+  a->scale_log2 = scale * kLog2e;
+  a->lse = lse;
+  a->delta = const_cast<float*>(delta);
+  a->o = static_cast<const __nv_bfloat16*>(out);
+  a->dO = static_cast<const __nv_bfloat16*>(dout);
+  a->dvres = static_cast<const __nv_bfloat16*>(dvres);
+  a->dq = a->dk = a->dv = static_cast<__nv_bfloat16*>(const_cast<void*>(dqkv));
+  return PSA_OK;
+}
+}  // namespace
+
+psa_status_t psa_attention_bwd_dq(const void* qkv, const void* out, const void* dout,
+                                  const float* lse, float* delta, void* dqkv, psa_shape_t s,
+                                  float scale, cudaStream_t st) {
+  CUtensorMap mqk, mv, mdo;
+  BwdArgs a;
+  psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
+  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &a);
+  if (e != PSA_OK) return e;
+  return from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, a, s.B * s.num_heads, s.key_dim, st));
+}
+
+psa_status_t psa_attention_bwd_dkdv(const void* qkv, const void* dout, const float* lse,
+                                    const float* delta, const void* dvres, void* dqkv,
+                                    psa_shape_t s, float scale, cudaStream_t st) {
+  CUtensorMap mqk, mv, mdo;
+  BwdArgs a;
+  psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
+  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk, &mv, &mdo, &a);
+  if (e != PSA_OK) return e;
+  return from_cuda(psa::launch_psa_bwd_dkdv(mqk, mv, mdo, a, s.B * s.num_heads, s.key_dim, st));
+}
+
+psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dout,
+                               const float* lse, const void* dvres, void* dqkv, void* ws,
+                               size_t ws_bytes, psa_shape_t s, float scale, cudaStream_t st) {
+  if (!ws) return PSA_ERR_INVALID_ARG;
+  psa_status_t e = check_shape(s);
+  if (e != PSA_OK) return e;
+  if (ws_bytes < psa_attention_bwd_workspace_size(s)) return PSA_ERR_INVALID_ARG;
+  float* delta = static_cast<float*>(ws);
+  // validate both launches completely before issuing either
+  CUtensorMap mqk, mv, mdo, mqk2, mv2, mdo2;
+  BwdArgs a_dq, a_kv;
+  e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
+  if (e == PSA_OK) e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
+  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &a_dq);
+  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk2, &mv2, &mdo2, &a_kv);
+  if (e != PSA_OK) return e;
+  const int BH = s.B * s.num_heads;
+  e = from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, a_dq, BH, s.key_dim, st));
+  if (e != PSA_OK) return e;
+  return from_cuda(psa::launch_psa_bwd_dkdv(mqk2, mv2, mdo2, a_kv, BH, s.key_dim, st));
+}
+
+}  // extern "C"

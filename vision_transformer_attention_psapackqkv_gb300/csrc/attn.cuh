@@ -1,0 +1,64 @@
+// attn.cuh -- launch interfaces of the attention kernels (forward and backward).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace psa {
+
+struct FwdArgs {
+  int N;             // sequence length (queries = keys)
+  int nh;            // heads per batch (NCHW layout)
+  int qkv_ch;        // channels per batch of the QKV tensor (NCHW layout)
+  int out_ch;        // channels per batch of the output (NCHW layout)
+  float scale_log2;  // scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;        // [BH, N] natural-log LSE, may be null
+};
+
+// bf16 tcgen05 forward.  Raw: 3-D maps over [BH, N, d] (box {d, 128, 1}).
+cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
+                                const CUtensorMap& mV, const FwdArgs& a, int BH, int d,
+                                cudaStream_t st);
+// NCHW: 2-D maps over [B*qkv_ch, N] with boxes {64, KD} (Q, K) and {64, 2*KD} (V).
+cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
+                                const FwdArgs& a, int BH, int KD, cudaStream_t st);
+
+cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
+                               float* lse, int BH, int N, int d, float scale, cudaStream_t st);
+cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, int nh, int KD,
+                               int N, float scale, cudaStream_t st);
+
+struct BwdArgs {
+  int N;
+  int nh;
+  int qkv_ch;        // NCHW: channels per batch of QKV / dQKV
+  int out_ch;        // NCHW: channels per batch of Out / dOut / dVres
+  float scale;       // softmax scale (natural units)
+  float scale_log2;  // scale * log2(e)
+  const float* lse;  // [BH, N] natural-log LSE from the forward
+  float* delta;      // [BH, N] rowsum(dO o O)
+  const __nv_bfloat16* o;     // raw: [BH, N, dv]; NCHW: out [B, out_ch, N]
+  const __nv_bfloat16* dO;    // raw: [BH, N, dv]; NCHW: dout [B, out_ch, N]
+  const __nv_bfloat16* dvres; // NCHW: optional gradient of the extracted V
+  __nv_bfloat16* dq;          // raw: [BH, N, dqk]; NCHW: dqkv [B, qkv_ch, N]
+  __nv_bfloat16* dk;          // raw: [BH, N, dqk]; NCHW: dqkv
+  __nv_bfloat16* dv;          // raw: [BH, N, dv];  NCHW: dqkv
+};
+
+// Raw layout maps: mQ/mK box {d, 128, 1}; mV/mDO box {d, 128, 1}.
+cudaError_t launch_fa2_bwd_dq(const CUtensorMap& mQ, const CUtensorMap& mK,
+                              const CUtensorMap& mV, const CUtensorMap& mDO,
+                              const BwdArgs& a, int BH, int d, cudaStream_t st);
+cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
+                                const CUtensorMap& mV, const CUtensorMap& mDO,
+                                const BwdArgs& a, int BH, int d, cudaStream_t st);
+// NCHW maps: mQK box {64, KD} and mV box {64, 2KD} over QKV; mDO box {64, 2KD} over dOut.
+cudaError_t launch_psa_bwd_dq(const CUtensorMap& mQK, const CUtensorMap& mV,
+                              const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
+                              cudaStream_t st);
+cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
+                                const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
+                                cudaStream_t st);
+
+}  // namespace psa

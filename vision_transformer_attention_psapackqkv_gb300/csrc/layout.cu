@@ -1,0 +1,191 @@
+// layout.cu -- PsaPackQkv, PsaExtractV, PsaMergeAttn and their adjoints
+// (vision-rs book, page "Custom Kernels", section "Position-Sensitive Attention (PSA)").
+//
+// All five are pure element permutations, so they move raw bits (T = uint16_t for
+// bf16, uint32_t for fp32) and are bit-exact by construction.  Two transposes
+// cover four of them:
+//   channels_to_rows: a block of KD channels x N positions (NCHW, positions
+//     contiguous) -> N rows x KD (row-major, KD contiguous).   pack, unmerge
+//   rows_to_channels: the inverse direction.                   unpack, merge
+// Each CTA moves a tile of KD channels x 64 positions through shared memory so
+// that both the global loads and the global stores are coalesced.  ExtractV is
+// a strided copy of contiguous per-head slabs in 16-byte vectors.
+#include <stdint.h>
+
+#include "layout.cuh"
+
+namespace psa {
+
+namespace {
+
+constexpr int kTileN = 64;
+constexpr int kThreads = 256;
+
+// One unit = one (b, head, plane s).  Source channel of element d:
+//   b * ch_per_batch + head * ch_per_head + s * KD + d   (NCHW side)
+// Row-major side: plane pointer rows[s], row (b * nh + head) * N + n.
+struct TransposeArgs {
+  const void* nchw_src;
+  void* nchw_dst;
+  const void* rows_src[4];
+  void* rows_dst[4];
+  int nh, KD, N, planes;
+  long long ch_per_batch, ch_per_head;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) channels_to_rows_kernel(TransposeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* tile = reinterpret_cast<T*>(smem_raw);  // [KD][kTileN + 1]
+  const int ntiles = (a.N + kTileN - 1) / kTileN;
+  const int unit = blockIdx.x / ntiles;
+  const int s = unit % a.planes;
+  const int bhd = unit / a.planes;  // b * nh + head
+  const int head = bhd % a.nh, b = bhd / a.nh;
+  const int n0 = (blockIdx.x % ntiles) * kTileN;
+  const int nvalid = min(kTileN, a.N - n0);
+  const T* src = static_cast<const T*>(a.nchw_src) +
+                 ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
+                  (long long)s * a.KD) * a.N;
+  for (int idx = threadIdx.x; idx < a.KD * kTileN; idx += kThreads) {
+    const int d = idx / kTileN, n = idx % kTileN;
+    if (n < nvalid) tile[d * (kTileN + 1) + n] = src[(long long)d * a.N + n0 + n];
+  }
+  __syncthreads();
+  T* dst = static_cast<T*>(a.rows_dst[s]) + ((long long)bhd * a.N + n0) * a.KD;
+  for (int idx = threadIdx.x; idx < nvalid * a.KD; idx += kThreads) {
+    const int n = idx / a.KD, d = idx % a.KD;
+    dst[idx] = tile[d * (kTileN + 1) + n];
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rows_to_channels_kernel(TransposeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* tile = reinterpret_cast<T*>(smem_raw);  // [KD][kTileN + 1]
+  const int ntiles = (a.N + kTileN - 1) / kTileN;
+  const int unit = blockIdx.x / ntiles;
+  const int s = unit % a.planes;
+  const int bhd = unit / a.planes;
+  const int head = bhd % a.nh, b = bhd / a.nh;
+  const int n0 = (blockIdx.x % ntiles) * kTileN;
+  const int nvalid = min(kTileN, a.N - n0);
+  const T* src = static_cast<const T*>(a.rows_src[s]) + ((long long)bhd * a.N + n0) * a.KD;
+  for (int idx = threadIdx.x; idx < nvalid * a.KD; idx += kThreads) {
+    const int n = idx / a.KD, d = idx % a.KD;
+    tile[d * (kTileN + 1) + n] = src[idx];
+  }
+  __syncthreads();
+  T* dst = static_cast<T*>(a.nchw_dst) +
+           ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
+            (long long)s * a.KD) * a.N;
+  for (int idx = threadIdx.x; idx < a.KD * kTileN; idx += kThreads) {
+    const int d = idx / kTileN, n = idx % kTileN;
+    if (n < nvalid) dst[(long long)d * a.N + n0 + n] = tile[d * (kTileN + 1) + n];
+  }
+}
+
+// Copies `slabs` contiguous slabs of slab_vec 16-byte vectors from src (slab
+// stride src_stride_vec) to dst (slab stride dst_stride_vec).
+__global__ void __launch_bounds__(kThreads)
+    strided_slab_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                             long long slabs, long long slab_vec, long long src_stride_vec,
+                             long long dst_stride_vec) {
+  const long long total = slabs * slab_vec;
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < total;
+       i += (long long)gridDim.x * kThreads) {
+    const long long sl = i / slab_vec, e = i % slab_vec;
+    dst[sl * dst_stride_vec + e] = src[sl * src_stride_vec + e];
+  }
+}
+
+template <typename T>
+cudaError_t launch_transpose(bool to_rows, const TransposeArgs& a, int B, cudaStream_t st) {
+  // one CTA per (64-position tile, unit); the flat index stays below 2^31 for
+  // every shape the entry points accept
+  const long long tiles = (long long)((a.N + kTileN - 1) / kTileN) * B * a.nh * a.planes;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)tiles);
+  const size_t smem = (size_t)a.KD * (kTileN + 1) * sizeof(T);
+  if (to_rows)
+    channels_to_rows_kernel<T><<<grid, kThreads, smem, st>>>(a);
+  else
+    rows_to_channels_kernel<T><<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t transpose(bool to_rows, const TransposeArgs& a, int B, int elem_bytes,
+                      cudaStream_t st) {
+  return elem_bytes == 2 ? launch_transpose<uint16_t>(to_rows, a, B, st)
+                         : launch_transpose<uint32_t>(to_rows, a, B, st);
+}
+
+}  // namespace
+
+cudaError_t launch_pack_qkv(const void* qkv, void* packed, int B, int nh, int KD, int N,
+                            int elem_bytes, cudaStream_t st) {
+  TransposeArgs a{};
+  a.nchw_src = qkv;
+  const long long plane = (long long)B * nh * N * KD * elem_bytes;
+  for (int s = 0; s < 4; ++s) a.rows_dst[s] = static_cast<char*>(packed) + s * plane;
+  a.nh = nh; a.KD = KD; a.N = N; a.planes = 4;
+  a.ch_per_batch = (long long)nh * 4 * KD;
+  a.ch_per_head = 4 * KD;
+  return transpose(true, a, B, elem_bytes, st);
+}
+
+cudaError_t launch_unpack_qkv(const void* packed, void* qkv, int B, int nh, int KD, int N,
+                              int elem_bytes, cudaStream_t st) {
+  TransposeArgs a{};
+  a.nchw_dst = qkv;
+  const long long plane = (long long)B * nh * N * KD * elem_bytes;
+  for (int s = 0; s < 4; ++s) a.rows_src[s] = static_cast<const char*>(packed) + s * plane;
+  a.nh = nh; a.KD = KD; a.N = N; a.planes = 4;
+  a.ch_per_batch = (long long)nh * 4 * KD;
+  a.ch_per_head = 4 * KD;
+  return transpose(false, a, B, elem_bytes, st);
+}
+
+cudaError_t launch_merge_attn(const void* o_lo, const void* o_hi, void* out, int B, int nh,
+                              int KD, int N, int elem_bytes, cudaStream_t st) {
+  TransposeArgs a{};
+  a.nchw_dst = out;
+  a.rows_src[0] = o_lo;
+  a.rows_src[1] = o_hi;
+  a.nh = nh; a.KD = KD; a.N = N; a.planes = 2;
+  a.ch_per_batch = (long long)nh * 2 * KD;
+  a.ch_per_head = 2 * KD;
+  return transpose(false, a, B, elem_bytes, st);
+}
+
+cudaError_t launch_unmerge_attn(const void* dout, void* do_lo, void* do_hi, int B, int nh,
+                                int KD, int N, int elem_bytes, cudaStream_t st) {
+  TransposeArgs a{};
+  a.nchw_src = dout;
+  a.rows_dst[0] = do_lo;
+  a.rows_dst[1] = do_hi;
+  a.nh = nh; a.KD = KD; a.N = N; a.planes = 2;
+  a.ch_per_batch = (long long)nh * 2 * KD;
+  a.ch_per_head = 2 * KD;
+  return transpose(true, a, B, elem_bytes, st);
+}
+
+cudaError_t launch_extract_v(const void* qkv, void* v, int B, int nh, int KD, int N,
+                             int elem_bytes, cudaStream_t st) {
+  // Per head the V section is 2*KD consecutive channels, i.e. one contiguous slab
+  // of 2*KD*N elements; slabs repeat every 4*KD*N elements in qkv and every
+  // 2*KD*N elements in v.  Callers guarantee 2*KD*N*elem_bytes % 16 == 0.
+  const long long slab_bytes = 2LL * KD * N * elem_bytes;
+  const long long slab_vec = slab_bytes / 16;
+  const long long slabs = (long long)B * nh;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(qkv) + slab_bytes);
+  const long long total = slabs * slab_vec;
+  long long blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  strided_slab_copy_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(
+      src, static_cast<uint4*>(v), slabs, slab_vec, 2 * slab_vec, slab_vec);
+  return cudaGetLastError();
+}
+
+}  // namespace psa
