@@ -153,6 +153,25 @@ psa_status_t psa_attention_bwd_dkdv(const void *qkv_nchw, const void *dout_nchw,
                                     const void *dvres_nchw, void *dqkv_nchw, psa_shape_t shape,
                                     float scale, cudaStream_t stream);
 
+/* psa_attention_bwd for callers that cannot allocate device memory when they run
+ * the backward (for example a plugin whose host framework owns all device
+ * allocations, or a latency-critical loop where cudaMalloc / cudaFree would
+ * synchronise the device).  The pages have no counterpart: this is a
+ * convenience of this library.  Same arguments, results and errors as
+ * psa_attention_bwd, minus the workspace.  The delta scratch lives in a fixed
+ * 4 MiB array inside the library's device memory, which every GPU that loads the
+ * library keeps until the process exits; B * num_heads * H * W may not exceed
+ * 1048576 (PSA_ERR_UNSUPPORTED otherwise).  The first call on each device, made
+ * with that device current, looks up the array's address; make that first call
+ * before any stream capture.  All calls share the one array: calls whose kernels
+ * overlap on the GPU (other streams, other threads) race on it, so serialise
+ * them.  Nothing in the array needs clearing between calls.  No allocation of
+ * any kind is made. */
+psa_status_t psa_attention_bwd_noalloc(const void *qkv_nchw, const void *out_nchw,
+                                       const void *dout_nchw, const float *lse,
+                                       const void *dvres_nchw, void *dqkv_nchw, psa_shape_t shape,
+                                       float scale, cudaStream_t stream);
+
 /* Bytes of device workspace psa_attention_bwd needs (0 for an invalid shape). */
 size_t psa_attention_bwd_workspace_size(psa_shape_t shape);
 

@@ -34,7 +34,7 @@ class PsaShape(ctypes.Structure):
 EXPORTED = (
     "psa_pack_qkv", "psa_unpack_qkv", "psa_extract_v", "psa_merge_attn", "psa_unmerge_attn",
     "flash_attn2_fwd", "flash_attn2_bwd_dq", "flash_attn2_bwd_dkdv", "psa_attention_fwd",
-    "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv",
+    "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv", "psa_attention_bwd_noalloc",
     "psa_attention_bwd_workspace_size", "psa_status_string",
     "psa_get_last_device_error",
 )
@@ -67,6 +67,7 @@ def load(path: str | None = None):
         "psa_attention_bwd": [P, P, P, P, P, P, P, Z, S, F, P],
         "psa_attention_bwd_dq": [P, P, P, P, P, P, S, F, P],
         "psa_attention_bwd_dkdv": [P, P, P, P, P, P, S, F, P],
+        "psa_attention_bwd_noalloc": [P, P, P, P, P, P, S, F, P],
         "psa_attention_bwd_workspace_size": [S],
         "psa_status_string": [I],
         "psa_get_last_device_error": [P],
@@ -186,6 +187,12 @@ def psa_attention_bwd_dq(qkv, out, dout, lse, delta, dqkv, shape: PsaShape, scal
 def psa_attention_bwd_dkdv(qkv, dout, lse, delta, dvres, dqkv, shape: PsaShape, scale: float, stream=None):
     _check("psa_attention_bwd_dkdv", load().psa_attention_bwd_dkdv(
         _ptr(qkv), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dvres), _ptr(dqkv), shape, float(scale),
+        _stream(stream)))
+
+
+def psa_attention_bwd_noalloc(qkv, out, dout, lse, dvres, dqkv, shape: PsaShape, scale: float, stream=None):
+    _check("psa_attention_bwd_noalloc", load().psa_attention_bwd_noalloc(
+        _ptr(qkv), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dvres), _ptr(dqkv), shape, float(scale),
         _stream(stream)))
 
 
