@@ -184,7 +184,7 @@ def run_ours(args, rank, world, local_rank):
                                  stream)
 
     parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
-    launches_per_step = 2 + 1 + 1  # forward attention + extract, dQ, dK/dV
+    launches_per_step = 1 + 1 + 1  # forward (with PsaExtractV fused), dQ, dK/dV
 
     def barrier():
         torch.cuda.synchronize()

@@ -92,7 +92,8 @@ psa_status_t check_fa2(const void* const* ptrs, int nptr, int BH, int n_ctx, int
     if (!ptrs[i]) return PSA_ERR_INVALID_ARG;
     if (!aligned16(ptrs[i])) return PSA_ERR_ALIGNMENT;
   }
-  if (BH <= 0 || n_ctx <= 0 || head_dim <= 0 || !isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (BH <= 0 || n_ctx <= 0 || head_dim <= 0 || !isfinite(scale) || !(scale > 0.f))
+    return PSA_ERR_INVALID_ARG;
   if (dtype != PSA_DTYPE_F32 && dtype != PSA_DTYPE_BF16) return PSA_ERR_INVALID_ARG;
   if (head_dim != 32 && head_dim != 64) return PSA_ERR_UNSUPPORTED;
   if ((long long)BH > 65535 || (long long)n_ctx > (1LL << 28)) return PSA_ERR_UNSUPPORTED;
@@ -187,16 +188,18 @@ psa_status_t flash_attn2_fwd(const void* q, const void* k, const void* v, void* 
     return from_cuda(psa::launch_fa2_fwd_f32((const float*)q, (const float*)k, (const float*)v,
                                              (float*)o, lse, BH, n_ctx, head_dim, scale, st));
   CUtensorMap mq, mk, mv;
-  if (!map_rows(&mq, q, BH, n_ctx, head_dim) || !map_rows(&mk, k, BH, n_ctx, head_dim) ||
-      !map_rows(&mv, v, BH, n_ctx, head_dim))
+  // the forward walks 128-query tiles against 64-key tiles
+  if (!map_rows(&mq, q, BH, n_ctx, head_dim, 128) || !map_rows(&mk, k, BH, n_ctx, head_dim, 64) ||
+      !map_rows(&mv, v, BH, n_ctx, head_dim, 64))
     return PSA_ERR_CUDA;
   FwdArgs a{};
   a.N = n_ctx;
+  a.BH = BH;
   a.nh = 1;
   a.scale_log2 = scale * kLog2e;
   a.out = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
-  return from_cuda(psa::launch_fa2_fwd_bf16(mq, mk, mv, a, BH, head_dim, st));
+  return from_cuda(psa::launch_fa2_fwd_bf16(mq, mk, mv, a, head_dim, st));
 }
 
 psa_status_t flash_attn2_bwd_dq(const void* q, const void* k, const void* v, const void* o,
@@ -256,7 +259,7 @@ psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_n
   if (!qkv || !out) return PSA_ERR_INVALID_ARG;
   psa_status_t e = check_shape(s);
   if (e != PSA_OK) return e;
-  if (!isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (!isfinite(scale) || !(scale > 0.f)) return PSA_ERR_INVALID_ARG;
   if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
   if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;
   if (!aligned16(qkv) || !aligned16(out) || (lse && !aligned16(lse)) ||
@@ -275,13 +278,16 @@ psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_n
       return PSA_ERR_CUDA;
     FwdArgs a{};
     a.N = N;
+    a.BH = s.B * nh;
     a.nh = nh;
     a.qkv_ch = nh * 4 * KD;
     a.out_ch = nh * 2 * KD;
+    a.vres_ch = nh * 2 * KD;
     a.scale_log2 = scale * kLog2e;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
-    e = from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, a, s.B * nh, KD, st));
+    a.vres = static_cast<__nv_bfloat16*>(v_nchw);  // PsaExtractV fused into the forward
+    return from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, a, KD, st));
   }
   if (e != PSA_OK || !v_nchw) return e;
   return from_cuda(psa::launch_extract_v(qkv, v_nchw, s.B, nh, KD, N, elem_bytes(s.dtype), st));
@@ -301,7 +307,7 @@ psa_status_t validate_bwd(const void* qkv, const void* dout, const float* lse, c
   if (!qkv || !dout || !lse || !dqkv || !delta || (need_out && !out)) return PSA_ERR_INVALID_ARG;
   psa_status_t e = check_shape(s);
   if (e != PSA_OK) return e;
-  if (!isfinite(scale)) return PSA_ERR_INVALID_ARG;
+  if (!isfinite(scale) || !(scale > 0.f)) return PSA_ERR_INVALID_ARG;
   if (s.dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
   if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
   if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;

@@ -8,21 +8,24 @@ namespace psa {
 
 struct FwdArgs {
   int N;             // sequence length (queries = keys)
+  int BH;            // heads x batch
   int nh;            // heads per batch (NCHW layout)
   int qkv_ch;        // channels per batch of the QKV tensor (NCHW layout)
   int out_ch;        // channels per batch of the output (NCHW layout)
-  float scale_log2;  // scale * log2(e)
+  int vres_ch;       // channels per batch of the extracted V (NCHW layout)
+  float scale_log2;  // scale * log2(e), > 0
   __nv_bfloat16* out;
   float* lse;        // [BH, N] natural-log LSE, may be null
+  __nv_bfloat16* vres;  // NCHW: PsaExtractV output [B, vres_ch, N], may be null
 };
 
-// bf16 tcgen05 forward.  Raw: 3-D maps over [BH, N, d] (box {d, 128, 1}).
+// bf16 tcgen05 forward, persistent grid.  Raw: 3-D maps over [BH, N, d] (box {d, 128, 1}).
 cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
-                                const CUtensorMap& mV, const FwdArgs& a, int BH, int d,
+                                const CUtensorMap& mV, const FwdArgs& a, int d,
                                 cudaStream_t st);
 // NCHW: 2-D maps over [B*qkv_ch, N] with boxes {64, KD} (Q, K) and {64, 2*KD} (V).
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
-                                const FwdArgs& a, int BH, int KD, cudaStream_t st);
+                                const FwdArgs& a, int KD, cudaStream_t st);
 
 cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
                                float* lse, int BH, int N, int d, float scale, cudaStream_t st);

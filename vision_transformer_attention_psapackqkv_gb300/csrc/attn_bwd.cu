@@ -27,54 +27,13 @@
 
 #include "attn.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace psa {
 
 namespace {
 
-__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
-  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kWaitLimitNs) break;
-}
-
 __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
-
-// Loads a tile of `rows_tile` sequence positions starting at pos0:
-//   raw:  one 3-D box {D, rows_tile, 1} at (0, pos0, bh)
-//   NCHW: rows_tile/64 boxes {64, D} at (pos0 + 64 b, ch)
-template <bool kNCHW, int D>
-__device__ __forceinline__ void load_tile(unsigned char* dst, const CUtensorMap* map,
-                                          uint64_t* bar, int rows_tile, int pos0, int bh,
-                                          int ch) {
-  if (kNCHW) {
-    for (int b = 0; b < rows_tile / 64; ++b)
-      tma_load_2d(dst + b * (D * 128), map, bar, pos0 + 64 * b, ch);
-  } else {
-    tma_load_3d(dst, map, bar, 0, pos0, bh);
-  }
-}
-
-// Shared-memory view of a tile loaded by load_tile.
-template <bool kNCHW, int D>
-__device__ __forceinline__ SmemTile tile_view(uint32_t base, int rows_tile) {
-  return kNCHW ? SmemTile{base, 128u, (uint32_t)D} : SmemTile{base, (uint32_t)(2 * D), (uint32_t)rows_tile};
-}
-
-// Operand whose M/N runs over sequence positions and K over the D channels.
-template <bool kNCHW>
-__device__ __forceinline__ uint64_t desc_pos_by_ch(const SmemTile& t, int k) {
-  return kNCHW ? desc_mnmajor(t, k) : desc_kmajor(t, k);
-}
-// Operand whose N runs over the D channels and K over sequence positions.
-template <bool kNCHW>
-__device__ __forceinline__ uint64_t desc_ch_by_pos(const SmemTile& t, int k) {
-  return kNCHW ? desc_kmajor(t, k) : desc_mnmajor(t, k);
-}
 
 // ====================================================================== dQ
 template <int DQK, int DV, bool kNCHW>

@@ -3,119 +3,192 @@
 // softmax over key tiles; the N x N score matrix only ever exists one 128 x 128
 // tile at a time, in tensor memory.
 //
-// bf16 path (tcgen05, sm_103a).  One CTA owns 128 query rows of one head and
-// walks the key tiles:
-//   warp 4   TMA producer: Q once, then K/V tiles into a 2-stage ring.
-//   warp 5   MMA issuer (one thread) and TMEM owner:
-//              S_j = Q K_j^T          -> TMEM (two 128-column buffers, so S_{j+1}
-//                                        is computed while S_j is in the softmax)
-//              O  += P_j V_j          -> TMEM (DV columns), P_j from shared memory
-//   warps 0-3 softmax, one thread per query row (= TMEM lane): read the S row,
-//            running max in the log2 domain, p = 2^(s - m) rounded to bf16 into
-//            P_j (K-major, 128-byte swizzle), running sum; O is rescaled in TMEM
-//            only when a row max grows by more than 2^8 (the result is exact
-//            either way because O and the sum share the stale max); epilogue
-//            O / l and LSE.
-// Layouts: kNCHW = false reads [BH, N, D] planes through 3-D tensor maps (Q, K
-// K-major; V MN-major for the P.V product); kNCHW = true reads the QKV conv
-// output [B, nh*4*KD, N] directly (Q, K MN-major; V K-major), which fuses
-// PsaPackQkv, the two V-half runs (one softmax, DV = 2*KD) and PsaMergeAttn.
+// bf16 path (tcgen05, sm_103a): a persistent kernel.  Each CTA runs NWG
+// independent 128-query-row pipelines ("slots"); slot s of the grid takes the
+// tiles t = s, s + S, s + 2S, ... (S = slots in the grid; tile t = head t / nqt,
+// query tile t % nqt).  Warp roles:
+//   warps 4w .. 4w+3   softmax of slot w: one thread per query row (= TMEM lane)
+//   warp 4*NWG         TMA producer: per slot, Q (double-buffered) and a 2-stage
+//                      K/V ring
+//   warp 4*NWG + 1     MMA issuer (one thread) and TMEM owner; per slot
+//                        S_k = Q K_k^T -> TMEM (128 columns)
+//                        O  += P_k V_k -> TMEM (DV columns), P_k from shared memory
+//                      S_{k+1} is issued as soon as the softmax has read S_k, so
+//                      it overlaps the exponentials of tile k.
+// Softmax: running max in the log2 domain; p = 2^(scale*log2e*s - m) rounded to
+// bf16 into P (K-major, 128-byte swizzle); O is rescaled in TMEM only when a row
+// max grows by more than 2^8 (exact either way, since O and the running sum
+// share the stale max).  Epilogue: O / l in the output layout and the LSE.
+// Layouts: kNCHW = false reads [BH, N, D] planes (Q, K K-major; V MN-major);
+// kNCHW = true reads the QKV conv output [B, nh*4*KD, N] directly (Q, K
+// MN-major; V K-major), which fuses PsaPackQkv, both V-half runs (one softmax,
+// DV = 2*KD), PsaMergeAttn, and optionally PsaExtractV (the slot whose query tile
+// index equals the key tile index copies that V tile out of shared memory).
 //
 // fp32 path (CUDA cores): the same online softmax with one thread per query
 // row and fp32 arithmetic throughout (a 1e-4 bound rules out tf32 inputs).
 #include <math.h>
 
+#include <algorithm>
+
 #include "attn.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace psa {
 
 namespace {
 
-template <int DQK, int DV, bool kNCHW>
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
 struct FwdCfg {
-  static constexpr int BM = 128, BN = 128, STAGES = 2;
-  static constexpr int kThreads = 192;
+  // 64-key tiles keep a whole S row in ~64 registers of its thread
+  static constexpr int BM = 128, BN = 64, STAGES = ST;
+  static_assert(ST >= 2 && ST <= 4 && QBUF >= 1 && QBUF <= 2, "buffering");
+  static constexpr int kSoftmaxWarps = 4 * NWG;
+  // control warps: TMA producer, MMA issuer (TMEM owner)
+  static constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1;
+  static constexpr int kThreads = 128 * NWG + 64;
   static constexpr uint32_t Q_BYTES = BM * DQK * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2;
   static constexpr uint32_t V_BYTES = BN * DV * 2;
   static constexpr uint32_t P_BYTES = BM * BN * 2;
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * K_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * V_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TM_S = 0, TM_O = 2 * BN;
-  static constexpr uint32_t QK_R = kNCHW ? 128 : 2 * DQK;
-  static constexpr uint32_t Q_ROWS = kNCHW ? DQK : BM;
-  static constexpr uint32_t K_ROWS = kNCHW ? DQK : BN;
-  static constexpr uint32_t V_R = kNCHW ? 128 : 2 * DV;
-  static constexpr uint32_t V_ROWS = kNCHW ? DV : BN;
+  // per-slot shared memory region
+  static constexpr uint32_t SL_Q = 0;
+  static constexpr uint32_t SL_K = SL_Q + QBUF * Q_BYTES;
+  static constexpr uint32_t SL_V = SL_K + STAGES * K_BYTES;
+  static constexpr uint32_t SL_P = SL_V + STAGES * V_BYTES;
+  static constexpr uint32_t SL_BYTES = SL_P + 2 * P_BYTES;  // P double-buffered
+  static constexpr uint32_t OFF_BAR = NWG * SL_BYTES;
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+  // tensor memory per slot w: S (BN columns) at TM_SLOT * w, O (DV columns) after it
+  static constexpr uint32_t TM_O = BN;
+  static constexpr uint32_t TM_SLOT = (BN + DV <= 128) ? 128 : 256;
+  static constexpr uint32_t TMEM_COLS = NWG * TM_SLOT < 32 ? 32 : NWG * TM_SLOT;
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(DQK % 16 == 0 && DV % 32 == 0 && DV <= 128, "tile shape");
-  static_assert(TM_O + DV <= TMEM_COLS, "tensor memory");
+  static_assert(SL_BYTES % 1024 == 0, "1024-byte aligned slot regions");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-constexpr float kLn2 = 0.69314718055994530942f;
+struct SlotBars {
+  uint64_t q_full[2], q_empty[2], kv_full[4], kv_empty[4];
+  uint64_t s_full, s_free, p_full[2], pv_done[2], o_free;  // P / P.V per P buffer
+};
 
-__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
-  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+// Loads this thread's NC-column S row from TMEM into registers with a single
+// wait (columns >= kend were not written by this tile's MMA and are not loaded).
+template <int NC>
+__device__ __forceinline__ void load_s_row(uint32_t srow, int kend, uint32_t (&s)[NC]) {
+  using Chunk = uint32_t[32];
+#pragma unroll
+  for (int c = 0; c < NC; c += 32)
+    if (c < kend) tmem_load32_async(srow + c, *reinterpret_cast<Chunk*>(s + c));
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < NC; c += 32) tmem_pin(*reinterpret_cast<Chunk*>(s + c));
 }
 
-// Drains (with a time limit only) a barrier phase that a TMA copy will complete.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+// Online-softmax step of one row held in registers.  Raw scores s (valid columns
+// only count; scale sl2 = scale*log2(e) > 0) become p = 2^(s*sl2 - m) packed as
+// bf16 pairs into the front half of s; m / l are the running max (log2 domain)
+// and sum.  Returns the factor the O accumulator must be scaled by (1 if the
+// max moved by no more than 2^8, in which case the stale max is kept).
+template <bool kFull, int NC>
+__device__ __forceinline__ float softmax_row(uint32_t (&s)[NC], int valid, float sl2, bool first,
+                                             float& m_run, float& l_run) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < NC; c += 4) {
+    if (kFull || c < valid) m0 = fmaxf(m0, __uint_as_float(s[c]));
+    if (kFull || c + 1 < valid) m1 = fmaxf(m1, __uint_as_float(s[c + 1]));
+    if (kFull || c + 2 < valid) m2 = fmaxf(m2, __uint_as_float(s[c + 2]));
+    if (kFull || c + 3 < valid) m3 = fmaxf(m3, __uint_as_float(s[c + 3]));
+  }
+  const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
+  float alpha = 1.f;
+  if (first) {
+    m_run = mx;
+  } else if (mx > m_run + 8.f) {
+    alpha = fast_exp2(m_run - mx);
+    m_run = mx;
+  }
+  const float nm = -m_run;
+  float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; c += 4) {
+    float p0 = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, nm));
+    float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 1]), sl2, nm));
+    float p2 = fast_exp2(fmaf(__uint_as_float(s[c + 2]), sl2, nm));
+    float p3 = fast_exp2(fmaf(__uint_as_float(s[c + 3]), sl2, nm));
+    if (!kFull) {
+      p0 = c < valid ? p0 : 0.f;
+      p1 = c + 1 < valid ? p1 : 0.f;
+      p2 = c + 2 < valid ? p2 : 0.f;
+      p3 = c + 3 < valid ? p3 : 0.f;
+    }
+    l0 += p0;
+    l1 += p1;
+    l2 += p2;
+    l3 += p3;
+    s[c / 2] = pack_bf16x2(p0, p1);
+    s[c / 2 + 1] = pack_bf16x2(p2, p3);
+  }
+  l_run = l_run * alpha + ((l0 + l1) + (l2 + l3));
+  return alpha;
 }
 
-template <int DQK, int DV, bool kNCHW>
-__global__ void __launch_bounds__(192, 1)
+// Number of tiles slot `slot` of `nslots` owns out of T.
+__device__ __forceinline__ int slot_tiles(int slot, int nslots, int T) {
+  return slot < T ? (T - slot + nslots - 1) / nslots : 0;
+}
+
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
+__global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQK,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = FwdCfg<DQK, DV, kNCHW>;
+  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V,
-                 sP = sbase + C::OFF_P;
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* pv_done = bars + 9;   // [2]
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  SlotBars* bars = reinterpret_cast<SlotBars*>(smem + C::OFF_BAR);
+  uint64_t* mma_done = reinterpret_cast<uint64_t*>(bars + NWG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * C::BM;
   const int N = args.N;
   const int nkv = (N + C::BN - 1) / C::BN;
-  // NCHW: channel row of this head's Q block in the 2-D [B*qkv_ch, N] view.
-  const int ch0 = kNCHW ? (bh / args.nh) * args.qkv_ch + (bh % args.nh) * 4 * DQK : 0;
+  const int nqt = (N + C::BM - 1) / C::BM;
+  const int T = args.BH * nqt;
+  const int nslots = gridDim.x * NWG;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(kv_full + i, 1);
-      mbar_init(kv_empty + i, 1);
-      mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
-      mbar_init(pv_done + i, 1);
+    for (int w = 0; w < NWG; ++w) {
+      SlotBars& b = bars[w];
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&b.q_full[i], 1);
+        mbar_init(&b.q_empty[i], 1);
+      }
+      for (int i = 0; i < C::STAGES; ++i) {
+        mbar_init(&b.kv_full[i], 1);
+        mbar_init(&b.kv_empty[i], 1);
+      }
+      mbar_init(&b.s_full, 1);
+      mbar_init(&b.s_free, 128);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&b.p_full[i], 128);
+        mbar_init(&b.pv_done[i], 1);
+      }
+      mbar_init(&b.o_free, 128);
     }
     mbar_init(mma_done, 1);
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -124,197 +197,307 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  int ntiles[NWG];
+  int max_tiles = 0;
+#pragma unroll
+  for (int w = 0; w < NWG; ++w) {
+    ntiles[w] = slot_tiles(blockIdx.x * NWG + w, nslots, T);
+    max_tiles = max(max_tiles, ntiles[w]);
+  }
+  // first channel row of head bh in the 2-D [B * qkv_ch, N] view of the QKV tensor
+  auto head_row = [&](int bh) { return (bh / args.nh) * args.qkv_ch + (bh % args.nh) * 4 * DQK; };
+
+  // the control warpgroup (producer, MMA issuer, two idle warps) hands registers
+  // to the softmax warpgroups
+  if (warp >= C::kSoftmaxWarps) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      if (kNCHW) {
-        for (int b = 0; b < C::BM / 64; ++b)
-          tma_load_2d(smem + C::OFF_Q + b * (DQK * 128), &tmQK, q_full, q0 + 64 * b, ch0);
-      } else {
-        tma_load_3d(smem + C::OFF_Q, &tmQK, q_full, 0, q0, bh);
-      }
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % C::STAGES;
-        if (j >= C::STAGES && !mbar_wait(&kv_empty[st], ((j / C::STAGES) - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::V_BYTES);
-        unsigned char* dK = smem + C::OFF_K + st * C::K_BYTES;
-        unsigned char* dV = smem + C::OFF_V + st * C::V_BYTES;
-        const int kv0 = j * C::BN;
-        if (kNCHW) {
-          for (int b = 0; b < C::BN / 64; ++b) {
-            tma_load_2d(dK + b * (DQK * 128), &tmK, &kv_full[st], kv0 + 64 * b, ch0 + DQK);
-            tma_load_2d(dV + b * (DV * 128), &tmV, &kv_full[st], kv0 + 64 * b, ch0 + 2 * DQK);
-          }
-        } else {
-          tma_load_3d(dK, &tmK, &kv_full[st], 0, kv0, bh);
-          tma_load_3d(dV, &tmV, &kv_full[st], 0, kv0, bh);
-        }
-        issued = j + 1;
-      }
-      if (*abort) {  // let copies still in flight land before the CTA exits
-        drain_wait(q_full, 0);
-        for (int j = (issued > C::STAGES ? issued - C::STAGES : 0); j < issued; ++j)
-          drain_wait(&kv_full[j % C::STAGES], (j / C::STAGES) & 1);
-      }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const SmemTile tQ{sQ, C::QK_R, C::Q_ROWS};
-      const uint32_t idPV = idesc_bf16_f32(128, DV, false, !kNCHW);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort)) return false;
-        tc_fence_after();
-        const SmemTile tP{sP + (i & 1) * C::P_BYTES, 128, C::BM};
-        const SmemTile tV{sV + (i % C::STAGES) * C::V_BYTES, C::V_R, C::V_ROWS};
-        const int valid = min(C::BN, N - i * C::BN);
-        const int kend = (valid + 15) & ~15;
-        for (int k = 0; k < kend; k += 16) {
-          const uint64_t a = desc_kmajor(tP, k);
-          const uint64_t b = kNCHW ? desc_kmajor(tV, k) : desc_mnmajor(tV, k);
-          mma_bf16(tmem + C::TM_O, a, b, idPV, (i > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(&pv_done[i & 1]);
-        mma_commit(&kv_empty[i % C::STAGES]);
+      bool ok = true;
+      int q_issued[NWG], kv_issued[NWG];
+#pragma unroll
+      for (int w = 0; w < NWG; ++w) q_issued[w] = kv_issued[w] = 0;
+      // Q of tile i goes to buffer i % QBUF; with two buffers, Q of tile i + 1 is
+      // fetched right after the first K/V tile of tile i so that it has landed
+      // when tile i ends
+      auto issue_q = [&](int w, int i) -> bool {
+        SlotBars& b = bars[w];
+        const int t = blockIdx.x * NWG + w + i * nslots;
+        const int bh = t / nqt, q0 = (t % nqt) * C::BM;
+        const int qb = i % QBUF;
+        if (i >= QBUF && !mbar_wait(&b.q_empty[qb], ((i / QBUF) - 1) & 1, abort)) return false;
+        mbar_arrive_expect_tx(&b.q_full[qb], C::Q_BYTES);
+        load_tile<kNCHW, DQK>(smem + w * C::SL_BYTES + C::SL_Q + qb * C::Q_BYTES, &tmQK,
+                              &b.q_full[qb], C::BM, q0, bh, kNCHW ? head_row(bh) : 0);
+        q_issued[w] = i + 1;
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, abort);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j % C::STAGES;
-        if (!mbar_wait(&kv_full[st], (j / C::STAGES) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const SmemTile tK{sK + st * C::K_BYTES, C::QK_R, C::K_ROWS};
-        const int valid = min(C::BN, N - j * C::BN);
-        const int nS = (valid + 15) & ~15;
-        const uint32_t idS = idesc_bf16_f32(128, nS, kNCHW, kNCHW);
-        const uint32_t dS = tmem + C::TM_S + (j & 1) * C::BN;
 #pragma unroll
-        for (int k = 0; k < DQK; k += 16) {
-          const uint64_t a = kNCHW ? desc_mnmajor(tQ, k) : desc_kmajor(tQ, k);
-          const uint64_t b = kNCHW ? desc_mnmajor(tK, k) : desc_kmajor(tK, k);
-          mma_bf16(dS, a, b, idS, k > 0 ? 1u : 0u);
+      for (int w = 0; w < NWG; ++w)
+        if (ok && ntiles[w] > 0) ok = issue_q(w, 0);
+      for (int i = 0; ok && i < max_tiles; ++i) {
+        if (QBUF == 1 && i > 0) {
+#pragma unroll
+          for (int w = 0; w < NWG; ++w)
+            if (ok && i < ntiles[w]) ok = issue_q(w, i);
         }
-        mma_commit(&s_full[j & 1]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        for (int j = 0; ok && j < nkv; ++j) {
+#pragma unroll
+          for (int w = 0; w < NWG; ++w) {
+            if (i >= ntiles[w]) continue;
+            SlotBars& b = bars[w];
+            const int t = blockIdx.x * NWG + w + i * nslots;
+            const int bh = t / nqt;
+            const int g = i * nkv + j, st = g % C::STAGES;
+            if (g >= C::STAGES && !mbar_wait(&b.kv_empty[st], ((g / C::STAGES) - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&b.kv_full[st], C::K_BYTES + C::V_BYTES);
+            unsigned char* sl = smem + w * C::SL_BYTES;
+            const int row = kNCHW ? head_row(bh) : 0;
+            load_tile<kNCHW, DQK>(sl + C::SL_K + st * C::K_BYTES, &tmK, &b.kv_full[st], C::BN,
+                                  j * C::BN, bh, row + DQK);
+            load_tile<kNCHW, DV>(sl + C::SL_V + st * C::V_BYTES, &tmV, &b.kv_full[st], C::BN,
+                                 j * C::BN, bh, row + 2 * DQK);
+            kv_issued[w] = g + 1;
+          }
+          if (QBUF == 2 && j == 0) {
+#pragma unroll
+            for (int w = 0; w < NWG; ++w)
+              if (ok && i + 1 < ntiles[w]) ok = issue_q(w, i + 1);
+          }
+        }
       }
-      if (ok) issue_pv(nkv - 1);
+      if (*abort) {
+        // let the copies issued last on every buffer land before the CTA exits
+#pragma unroll
+        for (int w = 0; w < NWG; ++w) {
+          for (int i = max(0, q_issued[w] - QBUF); i < q_issued[w]; ++i)
+            drain_wait(&bars[w].q_full[i % QBUF], (i / QBUF) & 1);
+          for (int g = max(0, kv_issued[w] - C::STAGES); g < kv_issued[w]; ++g)
+            drain_wait(&bars[w].kv_full[g % C::STAGES], (g / C::STAGES) & 1);
+        }
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // descriptors of buffer 0 / stage 0 of slot 0; the others are fixed offsets
+      const uint64_t dQ0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_Q, C::BM), 0);
+      const uint64_t dK0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_K, C::BN), 0);
+      const uint64_t dP0 = desc_kmajor(SmemTile{sbase + C::SL_P, 128, C::BM}, 0);
+      const uint64_t dV0 = desc_ch_by_pos<kNCHW>(tile_view<kNCHW, DV>(sbase + C::SL_V, C::BN), 0);
+      constexpr uint64_t kStepQK = kstep_pos_by_ch<kNCHW, DQK>();
+      constexpr uint64_t kStepP = 32 >> 4, kStepV = kstep_ch_by_pos<kNCHW, DV>();
+      const uint32_t idS_full = idesc_bf16_f32(128, C::BN, kNCHW, kNCHW);
+      const uint32_t idPV = idesc_bf16_f32(128, DV, false, !kNCHW);
+      auto issue_s = [&](int w, int i, int j) -> bool {
+        SlotBars& b = bars[w];
+        const int k = i * nkv + j;
+        if ((j == 0 && !mbar_wait(&b.q_full[i % QBUF], (i / QBUF) & 1, abort)) ||
+            !mbar_wait(&b.kv_full[k % C::STAGES], (k / C::STAGES) & 1, abort) ||
+            (k >= 1 && !mbar_wait(&b.s_free, (k - 1) & 1, abort)))
+          return false;
+        tc_fence_after();
+        const uint64_t slot_off = (uint64_t)(w * C::SL_BYTES) >> 4;
+        const uint64_t dQ = dQ0 + slot_off + (uint64_t)((i % QBUF) * C::Q_BYTES >> 4);
+        const uint64_t dK = dK0 + slot_off + (uint64_t)((k % C::STAGES) * C::K_BYTES >> 4);
+        const int valid = min(C::BN, N - j * C::BN);
+        const uint32_t idS =
+            valid == C::BN ? idS_full : idesc_bf16_f32(128, (valid + 15) & ~15, kNCHW, kNCHW);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_bf16(tmem + w * C::TM_SLOT, dQ + kk * kStepQK, dK + kk * kStepQK, idS,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(&b.s_full);
+        if (j == nkv - 1) mma_commit(&b.q_empty[i % QBUF]);
+        return true;
+      };
+      auto issue_pv = [&](int w, int i, int j) -> bool {
+        SlotBars& b = bars[w];
+        const int k = i * nkv + j;
+        if (!mbar_wait(&b.p_full[k & 1], (k >> 1) & 1, abort) ||
+            (j == 0 && i >= 1 && !mbar_wait(&b.o_free, (i - 1) & 1, abort)))
+          return false;
+        tc_fence_after();
+        const uint64_t slot_off = (uint64_t)(w * C::SL_BYTES) >> 4;
+        const uint64_t dP = dP0 + slot_off + (uint64_t)((k & 1) * C::P_BYTES >> 4);
+        const uint64_t dV = dV0 + slot_off + (uint64_t)((k % C::STAGES) * C::V_BYTES >> 4);
+        const uint32_t tO = tmem + w * C::TM_SLOT + C::TM_O;
+        const int valid = min(C::BN, N - j * C::BN);
+        if (valid == C::BN) {
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_bf16(tO, dP + kk * kStepP, dV + kk * kStepV, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk * 16 < valid; ++kk)
+            mma_bf16(tO, dP + kk * kStepP, dV + kk * kStepV, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&b.pv_done[k & 1]);
+        mma_commit(&b.kv_empty[k % C::STAGES]);
+        return true;
+      };
+      bool ok = true;
+      for (int i = 0; ok && i < max_tiles; ++i) {
+        for (int w = 0; ok && w < NWG; ++w)
+          if (i < ntiles[w]) ok = issue_s(w, i, 0);
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j + 1 < nkv)
+            for (int w = 0; ok && w < NWG; ++w)
+              if (i < ntiles[w]) ok = issue_s(w, i, j + 1);
+          for (int w = 0; ok && w < NWG; ++w)
+            if (i < ntiles[w]) ok = issue_pv(w, i, j);
+        }
+      }
       mma_commit(mma_done);
       drain_wait(mma_done, 0);  // every MMA retired before TMEM is released
     }
+  }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int r = threadIdx.x;  // query row within the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int w = warp >> 2;               // slot
+    const int r = threadIdx.x - 128 * w;   // query row within the tile = TMEM lane
+    const int wq = warp & 3;               // warp within the slot
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + w * C::TM_SLOT, tO = tS + C::TM_O;
+    const uint32_t sl = sbase + w * C::SL_BYTES;
+    SlotBars& b = bars[w];
     const float sl2 = args.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    const int my_tiles = slot_tiles(blockIdx.x * NWG + w, nslots, T);
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[C::BN];
-#pragma unroll
-      for (int c = 0; c < C::BN; c += 32)
-        tmem_load32(tmem + lane_base + C::TM_S + sb * C::BN + c,
-                    *reinterpret_cast<float(*)[32]>(s + c));
-      const int valid = min(C::BN, N - j * C::BN);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < C::BN; ++c) {
-        s[c] = (c < valid) ? s[c] * sl2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
-      }
-      bool need = false;
-      if (j == 0)
-        m_run = mx;
-      else
-        need = mx > m_run + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
-        if (need) m_run = mx;
-        l_run *= alpha;
-        if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) {
+    for (int i = 0; ok && i < my_tiles; ++i) {
+      const int t = blockIdx.x * NWG + w + i * nslots;
+      const int bh = t / nqt, qt = t % nqt, q0 = qt * C::BM;
+      const bool active = wq * 32 < N - q0;  // the warp has live rows
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        const int k = i * nkv + j;
+        const int valid = min(C::BN, N - j * C::BN);
+        const int kend = (valid + 15) & ~15;
+        if (!mbar_wait(&b.s_full, k & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (kNCHW && args.vres != nullptr && (j * C::BN) / C::BM == qt) {
+          // PsaExtractV: the slot whose query tile covers key tile j copies V tile j
+          // (rows = DV channels, BN/64 boxes of 64 positions) from shared memory to
+          // the NCHW output.  The stage stays resident until this slot's P_k is
+          // handed over.
+          if (!mbar_wait(&b.kv_full[k % C::STAGES], (k / C::STAGES) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          constexpr int kBoxes = C::BN / 64;
+          const uint32_t vb = sl + C::SL_V + (k % C::STAGES) * C::V_BYTES;
+          for (int e = r; e < DV * kBoxes; e += 128) {
+            const int ch = e / kBoxes, box = e % kBoxes;
+            const int pos0 = j * C::BN + box * 64;
+            __nv_bfloat16* dst = args.vres +
+                ((long long)(bh / args.nh) * args.vres_ch + (bh % args.nh) * DV + ch) * N + pos0;
 #pragma unroll
-        for (int c = 0; c < DV; c += 32) {
-          float o[32];
-          tmem_load32(tmem + lane_base + C::TM_O + c, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_store32(tmem + lane_base + C::TM_O + c, o);
+            for (int c8 = 0; c8 < 8; ++c8) {
+              if (pos0 + c8 * 8 < N) {
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(vb + box * (DV * 128) + swizzled_offset(ch, c8, 128)));
+                *reinterpret_cast<uint4*>(dst + c8 * 8) = v;
+              }
+            }
+          }
         }
+        // the whole S row goes to registers at once, so the S buffer is handed back
+        // to the MMA warp (which starts S_{k+1}) before the exponentials
+        uint32_t s[C::BN];
+        if (active) load_s_row(tS + lane_base, kend, s);
+        tc_fence_before();
+        mbar_arrive(&b.s_free);
+        float alpha = 1.f;
+        if (active)
+          alpha = valid == C::BN ? softmax_row<true, C::BN>(s, valid, sl2, j == 0, m_run, l_run)
+                                 : softmax_row<false, C::BN>(s, valid, sl2, j == 0, m_run, l_run);
+        // P buffer k & 1 was last read by P.V of k - 2
+        if (k >= 2 && !mbar_wait(&b.pv_done[k & 1], ((k >> 1) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (active) {
+          const uint32_t pbuf = sl + C::SL_P + (k & 1) * C::P_BYTES;
+#pragma unroll
+          for (int ch = 0; ch < C::BN / 8; ++ch)
+            if (ch * 8 < kend)
+              st_shared_v4(pbuf + (ch >> 3) * (C::BM * 128) + swizzled_offset(r, ch & 7, 128),
+                           s[ch * 4], s[ch * 4 + 1], s[ch * 4 + 2], s[ch * 4 + 3]);
+          // O may only be rescaled once every earlier P.V has landed in it
+          if (__any_sync(0xffffffffu, alpha != 1.f) &&
+              !mbar_wait(&b.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < DV; c += 32) {
+              float o[32];
+              tmem_load32(tO + lane_base + c, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_store32(tO + lane_base + c, o);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&b.p_full[k & 1]);
       }
-      if (j >= 2 && !mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1, abort)) {
+      if (!ok) break;
+      // epilogue: O / l in the output layout, LSE in natural-log units
+      const int klast = i * nkv + nkv - 1;
+      if (!mbar_wait(&b.pv_done[klast & 1], (klast >> 1) & 1, abort)) {
         ok = false;
         break;
       }
-      const uint32_t prow = sP + sb * C::P_BYTES;
-      float ls = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < C::BN / 8; ++ch) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(s[ch * 8 + e] - m_run);
-          ls += p[e];
-        }
-        st_shared_v4(prow + (ch >> 3) * (C::BM * 128) + swizzled_offset(r, ch & 7, 128),
-                     pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                     pack_bf16x2(p[6], p[7]));
-      }
-      l_run += ls;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[sb]);
-    }
-    // epilogue: O / l in the output layout, LSE in natural-log units
-    if (ok && mbar_wait(&pv_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1, abort)) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      const int q = q0 + r;
-      const bool live = q < N;
+      if (active) {
+        const float inv_l = 1.f / l_run;
+        const int q = q0 + r;
+        const bool live = q < N;
 #pragma unroll
-      for (int c = 0; c < DV; c += 32) {
-        float o[32];
-        tmem_load32(tmem + lane_base + C::TM_O + c, o);
-        if (live) {
-          if (kNCHW) {
-            const int b = bh / args.nh, hd = bh % args.nh;
-            __nv_bfloat16* dst =
-                args.out + ((long long)b * args.out_ch + hd * DV + c) * N + q;
+        for (int c = 0; c < DV; c += 32) {
+          float o[32];
+          tmem_load32(tO + lane_base + c, o);
+          if (live) {
+            if (kNCHW) {
+              __nv_bfloat16* dst = args.out +
+                  ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + c) * N + q;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(o[e] * inv_l);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + c);
+              for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(o[e] * inv_l);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + c);
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              dst[e / 8] = make_uint4(pack_bf16x2(o[e] * inv_l, o[e + 1] * inv_l),
-                                      pack_bf16x2(o[e + 2] * inv_l, o[e + 3] * inv_l),
-                                      pack_bf16x2(o[e + 4] * inv_l, o[e + 5] * inv_l),
-                                      pack_bf16x2(o[e + 6] * inv_l, o[e + 7] * inv_l));
+              for (int e = 0; e < 32; e += 8)
+                dst[e / 8] = make_uint4(pack_bf16x2(o[e] * inv_l, o[e + 1] * inv_l),
+                                        pack_bf16x2(o[e + 2] * inv_l, o[e + 3] * inv_l),
+                                        pack_bf16x2(o[e + 4] * inv_l, o[e + 5] * inv_l),
+                                        pack_bf16x2(o[e + 6] * inv_l, o[e + 7] * inv_l));
+            }
           }
         }
+        if (live && args.lse) args.lse[(long long)bh * N + q] = (m_run + log2f(l_run)) * kLn2;
       }
-      if (live && args.lse) args.lse[(long long)bh * N + q] = (m_run + log2f(l_run)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&b.o_free);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -392,16 +575,31 @@ __global__ void __launch_bounds__(128)
   if (lse) lse[(long long)bh * N + i] = m + logf(l);
 }
 
-template <int DQK, int DV, bool kNCHW>
+
+int sm_count() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    return v;
+  }();
+  return n;
+}
+
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
 cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUtensorMap& mV,
-                      const FwdArgs& a, int BH, cudaStream_t st) {
-  using C = FwdCfg<DQK, DV, kNCHW>;
-  auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW>;
+                      const FwdArgs& a, cudaStream_t st) {
+  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST>;
+  auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW, NWG, QBUF, ST>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
-  dim3 grid((a.N + C::BM - 1) / C::BM, BH);
-  kern<<<grid, C::kThreads, C::SMEM_BYTES, st>>>(mQK, mK, mV, a);
+  // persistent grid: one CTA per SM with two slots, or two single-slot CTAs per SM
+  const long long T = (long long)a.BH * ((a.N + C::BM - 1) / C::BM);
+  const long long per_sm = NWG == 1 ? 2 : 1;
+  const long long ctas = std::min<long long>(per_sm * sm_count(), (T + NWG - 1) / NWG);
+  kern<<<(unsigned)ctas, C::kThreads, C::SMEM_BYTES, st>>>(mQK, mK, mV, a);
   return cudaGetLastError();
 }
 
@@ -415,19 +613,22 @@ cudaError_t launch_f32(const float* q, const float* k, const float* v, float* ou
   return cudaGetLastError();
 }
 
+
 }  // namespace
 
 cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
-                                const CUtensorMap& mV, const FwdArgs& a, int BH, int d,
+                                const CUtensorMap& mV, const FwdArgs& a, int d,
                                 cudaStream_t st) {
-  if (d == 32) return launch_tc<32, 32, false>(mQ, mK, mV, a, BH, st);
-  return launch_tc<64, 64, false>(mQ, mK, mV, a, BH, st);
+  // <DQK, DV, layout, slots per CTA, Q buffers, K/V stages>: two CTAs per SM, each
+  // within half of the SM's shared memory and tensor memory
+  if (d == 32) return launch_tc<32, 32, false, 1, 2, 4>(mQ, mK, mV, a, st);
+  return launch_tc<64, 64, false, 1, 2, 2>(mQ, mK, mV, a, st);
 }
 
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
-                                const FwdArgs& a, int BH, int KD, cudaStream_t st) {
-  if (KD == 32) return launch_tc<32, 64, true>(mQK, mQK, mV, a, BH, st);
-  return launch_tc<64, 128, true>(mQK, mQK, mV, a, BH, st);
+                                const FwdArgs& a, int KD, cudaStream_t st) {
+  if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4>(mQK, mQK, mV, a, st);
+  return launch_tc<64, 128, true, 1, 1, 2>(mQK, mQK, mV, a, st);
 }
 
 cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
