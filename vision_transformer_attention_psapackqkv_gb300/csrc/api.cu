@@ -217,6 +217,7 @@ psa_status_t flash_attn2_bwd_dq(const void* q, const void* k, const void* v, con
     return PSA_ERR_CUDA;
   BwdArgs a{};
   a.N = n_ctx;
+  a.BH = BH;
   a.nh = 1;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
@@ -243,6 +244,7 @@ psa_status_t flash_attn2_bwd_dkdv(const void* q, const void* k, const void* v, c
     return PSA_ERR_CUDA;
   BwdArgs a{};
   a.N = n_ctx;
+  a.BH = BH;
   a.nh = 1;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
@@ -331,6 +333,7 @@ psa_status_t make_bwd(const void* qkv, const void* dout, const float* lse, const
     return PSA_ERR_CUDA;
   *a = BwdArgs{};
   a->N = N;
+  a->BH = s.B * nh;
   a->nh = nh;
   a->qkv_ch = nh * 4 * KD;
   a->out_ch = nh * 2 * KD;

@@ -32,8 +32,21 @@ cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, f
 cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, int nh, int KD,
                                int N, float scale, cudaStream_t st);
 
+// Multiprocessor count of the current device (queried once; persistent grids).
+inline int device_sm_count() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    return v;
+  }();
+  return n;
+}
+
 struct BwdArgs {
   int N;
+  int BH;
   int nh;
   int qkv_ch;        // NCHW: channels per batch of QKV / dQKV
   int out_ch;        // NCHW: channels per batch of Out / dOut / dVres

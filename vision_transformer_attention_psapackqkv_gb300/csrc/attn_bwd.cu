@@ -8,22 +8,29 @@
 // No atomics: every output element is produced by exactly one CTA, so results
 // are bitwise reproducible.
 //
-// dQ kernel: one CTA per (128 query rows, head), walking 64-key tiles.
-//   prologue (softmax warps): delta of its row from O and dO, written out for the
+// Both kernels are persistent (CTAs take work units round-robin) with 192
+// threads: warps 0-3 do the elementwise work, one thread per tile row (= TMEM
+// lane); warp 4 is the TMA producer; warp 5 issues every tcgen05.mma from
+// precomputed shared-memory descriptors and owns TMEM.  Each thread loads its
+// whole 64-column S / dP row pair into registers with one wait and hands the TMEM
+// back at once, so the next tile's MMAs overlap its exponentials.
+//
+// dQ kernel: unit = (head, 128 query rows); walks 64-key tiles.
+//   prologue (row threads): delta of the row from O and dO, written out for the
 //     dK/dV kernel, which therefore runs after this one.
-//   MMA:  S_j = Q K_j^T and dP_j = dO V_j^T into TMEM (double-buffered, 4 x 64
-//         columns), then dQ += dS_j K_j (dS_j bf16 from shared memory).
-//   softmax warps: one thread per query row, P and dS of 64 keys per tile.
-// dK/dV kernel: one CTA per (128 key rows, head), walking 64-query tiles.
-//   MMA:  S^T_i = K Q_i^T and dP^T_i = V dO_i^T into TMEM (double-buffered), then
-//         dV += P^T_i dO_i and dK += dS^T_i Q_i (P^T, dS^T bf16 from shared memory).
-//   softmax warps: one thread per key row; lse and delta of the 64 query columns
-//         come from shared memory, written there by the producer warp.
+//   MMA:  S = Q K_j^T, dP = dO V_j^T (TMEM, 64 columns each); dQ += dS_j K_j
+//         (dS_j bf16 in shared memory, double-buffered).
+// dK/dV kernel: unit = (head, 128 key rows); walks 64-query tiles.
+//   MMA:  S^T = K Q_i^T, dP^T = V dO_i^T; dV += P^T_i dO_i, dK += dS^T_i Q_i.
+//   lse and delta of the 64 query columns come from shared memory, written
+//   there by the producer warp next to each Q / dO stage.
 // Layouts as in the forward: kNCHW = false uses [BH, N, d] planes, kNCHW = true
 // reads QKV / Out / dOut in NCHW and writes dQKV in NCHW (the adjoints of
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing; the optional
 // PsaExtractV gradient is added into the V channels).
 #include <math.h>
+
+#include <algorithm>
 
 #include "attn.cuh"
 #include "ptx.cuh"
@@ -33,66 +40,108 @@ namespace psa {
 
 namespace {
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
 
+__device__ __forceinline__ int unit_count(int slot, int nslots, int T) {
+  return slot < T ? (T - slot + nslots - 1) / nslots : 0;
+}
+
+// Loads a 64-column S row and the matching dP row (TMEM columns tS, tP) with
+// one wait; columns >= kend were not written and are not loaded.
+__device__ __forceinline__ void load_sp_rows(uint32_t tS, uint32_t tP, int kend,
+                                             uint32_t (&s)[64], uint32_t (&p)[64]) {
+  using Chunk = uint32_t[32];
+  tmem_load32_async(tS, *reinterpret_cast<Chunk*>(s));
+  tmem_load32_async(tP, *reinterpret_cast<Chunk*>(p));
+  if (kend > 32) {
+    tmem_load32_async(tS + 32, *reinterpret_cast<Chunk*>(s + 32));
+    tmem_load32_async(tP + 32, *reinterpret_cast<Chunk*>(p + 32));
+  }
+  tmem_wait_ld();
+  tmem_pin(*reinterpret_cast<Chunk*>(s));
+  tmem_pin(*reinterpret_cast<Chunk*>(p));
+  tmem_pin(*reinterpret_cast<Chunk*>(s + 32));
+  tmem_pin(*reinterpret_cast<Chunk*>(p + 32));
+}
+
+// Stores 8 packed bf16x2 words per 16-byte chunk of a 128-row, 64-column K-major
+// tile with the 128-byte swizzle (row r, chunks below kend / 8).
+__device__ __forceinline__ void store_row64(uint32_t tile, int r, int kend, const uint32_t* w) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch)
+    if (ch * 8 < kend)
+      st_shared_v4(tile + swizzled_offset(r, ch, 128), w[ch * 4], w[ch * 4 + 1], w[ch * 4 + 2],
+                   w[ch * 4 + 3]);
+}
+
 // ====================================================================== dQ
-template <int DQK, int DV, bool kNCHW>
+template <int DQK, int DV, bool kNCHW, int QBUF, int ST, int CPS>
 struct DqCfg {
-  static constexpr int BM = 128, BN = 64, STAGES = 2, kThreads = 192;
+  static constexpr int BM = 128, BN = 64, kThreads = 192, STAGES = ST;
+  static_assert(QBUF >= 1 && QBUF <= 2 && ST >= 2 && ST <= 4, "buffering");
   static constexpr uint32_t Q_BYTES = BM * DQK * 2, DO_BYTES = BM * DV * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2, V_BYTES = BN * DV * 2;
   static constexpr uint32_t DS_BYTES = BM * BN * 2;
-  static constexpr uint32_t OFF_Q = 0, OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_K = OFF_DO + DO_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * K_BYTES;
-  static constexpr uint32_t OFF_DS = OFF_V + STAGES * V_BYTES;
+  static constexpr uint32_t OFF_Q = 0, OFF_DO = OFF_Q + QBUF * Q_BYTES;
+  static constexpr uint32_t OFF_K = OFF_DO + QBUF * DO_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + ST * K_BYTES;
+  static constexpr uint32_t OFF_DS = OFF_V + ST * V_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_BYTES;
-  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM: S[b] at 128 b, dP[b] at 128 b + 64, dQ at 256
-  static constexpr uint32_t TM_DQ = 256;
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(TM_DQ + DQK <= TMEM_COLS, "tensor memory");
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+  // TMEM: S at 0, dP at 64, dQ at 128
+  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128;
+  static constexpr uint32_t TMEM_COLS = TM_DQ + DQK <= 256 ? 256 : 512;
+  static_assert(SMEM_BYTES <= 227 * 1024 && (CPS == 1 || SMEM_BYTES <= 113 * 1024), "shared memory");
+  static_assert(CPS == 1 || TMEM_COLS <= 256, "tensor memory");
 };
 
-template <int DQK, int DV, bool kNCHW>
-__global__ void __launch_bounds__(192, 1)
+struct DqBars {
+  uint64_t q_full[2], q_empty[2], kv_full[4], kv_empty[4];
+  uint64_t s_full, s_free, ds_full[2], ds_free[2], dq_free, mma_done;
+};
+
+template <int DQK, int DV, bool kNCHW, int QBUF, int ST, int CPS>
+__global__ void __launch_bounds__(192, CPS)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmDO, const BwdArgs args) {
-  using C = DqCfg<DQK, DV, kNCHW>;
+  using C = DqCfg<DQK, DV, kNCHW, QBUF, ST, CPS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t sbase = smem_addr(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* ds_full = bars + 7;   // [2]
-  uint64_t* ds_free = bars + 9;   // [2]
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  DqBars& b = *reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&b + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y, q0 = blockIdx.x * C::BM, N = args.N;
+  const int N = args.N;
   const int nkv = (N + C::BN - 1) / C::BN;
-  const int b = bh / args.nh, hd = bh % args.nh;
-  const int ch0 = kNCHW ? b * args.qkv_ch + hd * 4 * DQK : 0;  // Q rows in the QKV view
-  const int och0 = kNCHW ? b * args.out_ch + hd * DV : 0;      // rows in the Out view
+  const int nqt = (N + C::BM - 1) / C::BM;
+  const int T = args.BH * nqt;
+  const int nunits = unit_count(blockIdx.x, gridDim.x, T);
+  auto unit_of = [&](int u) { return (int)blockIdx.x + u * (int)gridDim.x; };
+  // first channel row of head bh in the QKV view / in the Out view
+  auto qkv_row = [&](int bh) { return kNCHW ? (bh / args.nh) * args.qkv_ch + (bh % args.nh) * 4 * DQK : 0; };
+  auto out_row = [&](int bh) { return kNCHW ? (bh / args.nh) * args.out_ch + (bh % args.nh) * DV : 0; };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(kv_full + i, 1);
-      mbar_init(kv_empty + i, 1);
-      mbar_init(s_full + i, 1);
-      mbar_init(ds_full + i, 128);
-      mbar_init(ds_free + i, 1);
+      mbar_init(&b.q_full[i], 1);
+      mbar_init(&b.q_empty[i], 1);
+      mbar_init(&b.ds_full[i], 128);
+      mbar_init(&b.ds_free[i], 1);
     }
-    mbar_init(mma_done, 1);
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&b.kv_full[i], 1);
+      mbar_init(&b.kv_empty[i], 1);
+    }
+    mbar_init(&b.s_full, 1);
+    mbar_init(&b.s_free, 128);
+    mbar_init(&b.dq_free, 128);
+    mbar_init(&b.mma_done, 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -106,165 +155,218 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
-      load_tile<kNCHW, DQK>(smem + C::OFF_Q, &tmQ, q_full, C::BM, q0, bh, ch0);
-      load_tile<kNCHW, DV>(smem + C::OFF_DO, &tmDO, q_full, C::BM, q0, bh, och0);
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % C::STAGES;
-        if (j >= C::STAGES && !mbar_wait(&kv_empty[st], ((j / C::STAGES) - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::V_BYTES);
-        load_tile<kNCHW, DQK>(smem + C::OFF_K + st * C::K_BYTES, &tmK, &kv_full[st], C::BN,
-                              j * C::BN, bh, ch0 + DQK);
-        load_tile<kNCHW, DV>(smem + C::OFF_V + st * C::V_BYTES, &tmV, &kv_full[st], C::BN,
-                             j * C::BN, bh, ch0 + 2 * DQK);
-        issued = j + 1;
+      bool ok = true;
+      int q_issued = 0, kv_issued = 0;
+      auto issue_q = [&](int u) -> bool {
+        const int t = unit_of(u), bh = t / nqt, q0 = (t % nqt) * C::BM;
+        const int qb = u % QBUF;
+        if (u >= QBUF && !mbar_wait(&b.q_empty[qb], ((u / QBUF) - 1) & 1, abort)) return false;
+        mbar_arrive_expect_tx(&b.q_full[qb], C::Q_BYTES + C::DO_BYTES);
+        load_tile<kNCHW, DQK>(smem + C::OFF_Q + qb * C::Q_BYTES, &tmQ, &b.q_full[qb], C::BM, q0, bh,
+                              qkv_row(bh));
+        load_tile<kNCHW, DV>(smem + C::OFF_DO + qb * C::DO_BYTES, &tmDO, &b.q_full[qb], C::BM, q0,
+                             bh, out_row(bh));
+        q_issued = u + 1;
+        return true;
+      };
+      if (nunits > 0) ok = issue_q(0);
+      for (int u = 0; ok && u < nunits; ++u) {
+        const int bh = unit_of(u) / nqt;
+        for (int j = 0; ok && j < nkv; ++j) {
+          const int g = u * nkv + j, st = g % C::STAGES;
+          if (g >= C::STAGES && !mbar_wait(&b.kv_empty[st], ((g / C::STAGES) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&b.kv_full[st], C::K_BYTES + C::V_BYTES);
+          load_tile<kNCHW, DQK>(smem + C::OFF_K + st * C::K_BYTES, &tmK, &b.kv_full[st], C::BN,
+                                j * C::BN, bh, qkv_row(bh) + DQK);
+          load_tile<kNCHW, DV>(smem + C::OFF_V + st * C::V_BYTES, &tmV, &b.kv_full[st], C::BN,
+                               j * C::BN, bh, qkv_row(bh) + 2 * DQK);
+          kv_issued = g + 1;
+          if (u + 1 < nunits && ((QBUF == 2 && j == 0) || (QBUF == 1 && j == nkv - 1)))
+            ok = issue_q(u + 1);
+        }
       }
       if (*abort) {
-        drain_wait(q_full, 0);
-        for (int j = (issued > C::STAGES ? issued - C::STAGES : 0); j < issued; ++j)
-          drain_wait(&kv_full[j % C::STAGES], (j / C::STAGES) & 1);
+        for (int u = max(0, q_issued - QBUF); u < q_issued; ++u)
+          drain_wait(&b.q_full[u % QBUF], (u / QBUF) & 1);
+        for (int g = max(0, kv_issued - C::STAGES); g < kv_issued; ++g)
+          drain_wait(&b.kv_full[g % C::STAGES], (g / C::STAGES) & 1);
       }
     }
   } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const SmemTile tQ = tile_view<kNCHW, DQK>(sbase + C::OFF_Q, C::BM);
-      const SmemTile tDO = tile_view<kNCHW, DV>(sbase + C::OFF_DO, C::BM);
-      const uint32_t idSP = idesc_bf16_f32(128, C::BN, kNCHW, kNCHW);
+      const uint64_t dQ0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_Q, C::BM), 0);
+      const uint64_t dDO0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DV>(sbase + C::OFF_DO, C::BM), 0);
+      const uint64_t dK0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_K, C::BN), 0);
+      const uint64_t dV0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DV>(sbase + C::OFF_V, C::BN), 0);
+      const uint64_t dKb0 = desc_ch_by_pos<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_K, C::BN), 0);
+      const uint64_t dDS0 = desc_kmajor(SmemTile{sbase + C::OFF_DS, 128, C::BM}, 0);
+      constexpr uint64_t kStepQK = kstep_pos_by_ch<kNCHW, DQK>(), kStepV = kstep_pos_by_ch<kNCHW, DV>();
+      constexpr uint64_t kStepKb = kstep_ch_by_pos<kNCHW, DQK>(), kStepDS = 32 >> 4;
+      const uint32_t idSP_full = idesc_bf16_f32(128, C::BN, kNCHW, kNCHW);
       const uint32_t idDQ = idesc_bf16_f32(128, DQK, false, !kNCHW);
-      auto issue_dq = [&](int i) -> bool {
-        if (!mbar_wait(&ds_full[i & 1], (i >> 1) & 1, abort)) return false;
+      auto issue_sdp = [&](int u, int j) -> bool {
+        const int k = u * nkv + j;
+        if ((j == 0 && !mbar_wait(&b.q_full[u % QBUF], (u / QBUF) & 1, abort)) ||
+            !mbar_wait(&b.kv_full[k % C::STAGES], (k / C::STAGES) & 1, abort) ||
+            (k >= 1 && !mbar_wait(&b.s_free, (k - 1) & 1, abort)))
+          return false;
         tc_fence_after();
-        const SmemTile tDS{sbase + C::OFF_DS + (i & 1) * C::DS_BYTES, 128, C::BM};
-        const SmemTile tK = tile_view<kNCHW, DQK>(sbase + C::OFF_K + (i % C::STAGES) * C::K_BYTES, C::BN);
-        const int valid = min(C::BN, N - i * C::BN);
-        const int kend = (valid + 15) & ~15;
-        for (int k = 0; k < kend; k += 16)
-          mma_bf16(tmem + C::TM_DQ, desc_kmajor(tDS, k), desc_ch_by_pos<kNCHW>(tK, k), idDQ,
-                   (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&ds_free[i & 1]);
-        mma_commit(&kv_empty[i % C::STAGES]);
+        const uint64_t dQ = dQ0 + (uint64_t)((u % QBUF) * C::Q_BYTES >> 4);
+        const uint64_t dDO = dDO0 + (uint64_t)((u % QBUF) * C::DO_BYTES >> 4);
+        const uint64_t dK = dK0 + (uint64_t)((k % C::STAGES) * C::K_BYTES >> 4);
+        const uint64_t dV = dV0 + (uint64_t)((k % C::STAGES) * C::V_BYTES >> 4);
+        const int valid = min(C::BN, N - j * C::BN);
+        const uint32_t idSP =
+            valid == C::BN ? idSP_full : idesc_bf16_f32(128, (valid + 15) & ~15, kNCHW, kNCHW);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_bf16(tmem + C::TM_S, dQ + kk * kStepQK, dK + kk * kStepQK, idSP, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_bf16(tmem + C::TM_DP, dDO + kk * kStepV, dV + kk * kStepV, idSP, kk > 0 ? 1u : 0u);
+        mma_commit(&b.s_full);
+        if (j == nkv - 1) mma_commit(&b.q_empty[u % QBUF]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, abort);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j % C::STAGES;
-        if (!mbar_wait(&kv_full[st], (j / C::STAGES) & 1, abort)) {
+      auto issue_dq = [&](int u, int j) -> bool {
+        const int k = u * nkv + j;
+        if (!mbar_wait(&b.ds_full[k & 1], (k >> 1) & 1, abort) ||
+            (j == 0 && u >= 1 && !mbar_wait(&b.dq_free, (u - 1) & 1, abort)))
+          return false;
+        tc_fence_after();
+        const uint64_t dDS = dDS0 + (uint64_t)((k & 1) * C::DS_BYTES >> 4);
+        const uint64_t dKb = dKb0 + (uint64_t)((k % C::STAGES) * C::K_BYTES >> 4);
+        const int valid = min(C::BN, N - j * C::BN);
+        for (int kk = 0; kk * 16 < valid; ++kk)
+          mma_bf16(tmem + C::TM_DQ, dDS + kk * kStepDS, dKb + kk * kStepKb, idDQ,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&b.ds_free[k & 1]);
+        mma_commit(&b.kv_empty[k % C::STAGES]);
+        return true;
+      };
+      bool ok = true;
+      for (int u = 0; ok && u < nunits; ++u) {
+        ok = issue_sdp(u, 0);
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j + 1 < nkv) ok = issue_sdp(u, j + 1);
+          if (ok) ok = issue_dq(u, j);
+        }
+      }
+      mma_commit(&b.mma_done);
+      drain_wait(&b.mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ row threads
+    const int r = threadIdx.x;
+    const int wq = warp;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float sl2 = args.scale_log2;
+    bool ok = true;
+    for (int u = 0; ok && u < nunits; ++u) {
+      const int t = unit_of(u), bh = t / nqt, q0 = (t % nqt) * C::BM;
+      const bool active = wq * 32 < N - q0;
+      const int q = q0 + r;
+      const bool live = q < N;
+      // delta of this row, and the row's lse in the log2 domain
+      float D = 0.f, lse2 = 0.f;
+      if (live) {
+        if (kNCHW) {
+          const __nv_bfloat16* o = args.o + (long long)out_row(bh) * N + q;
+          const __nv_bfloat16* g = args.dO + (long long)out_row(bh) * N + q;
+#pragma unroll 8
+          for (int c = 0; c < DV; ++c) D = fmaf(bf(o[(long long)c * N]), bf(g[(long long)c * N]), D);
+        } else {
+          const uint4* o = reinterpret_cast<const uint4*>(args.o + ((long long)bh * N + q) * DV);
+          const uint4* g = reinterpret_cast<const uint4*>(args.dO + ((long long)bh * N + q) * DV);
+#pragma unroll
+          for (int c = 0; c < DV / 8; ++c) {
+            const uint4 ov = o[c], gv = g[c];
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+              D = fmaf(of.x, gf.x, D);
+              D = fmaf(of.y, gf.y, D);
+            }
+          }
+        }
+        args.delta[(long long)bh * N + q] = D;
+        lse2 = args.lse[(long long)bh * N + q] * kLog2e;
+      }
+      for (int j = 0; j < nkv; ++j) {
+        const int k = u * nkv + j;
+        const int valid = min(C::BN, N - j * C::BN);
+        const int kend = (valid + 15) & ~15;
+        if (!mbar_wait(&b.s_full, k & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const SmemTile tK = tile_view<kNCHW, DQK>(sbase + C::OFF_K + st * C::K_BYTES, C::BN);
-        const SmemTile tV = tile_view<kNCHW, DV>(sbase + C::OFF_V + st * C::V_BYTES, C::BN);
-        const uint32_t dS = tmem + (j & 1) * 128, dP = dS + 64;
+        uint32_t s[64], p[64];
+        if (active) load_sp_rows(tmem + lane_base + C::TM_S, tmem + lane_base + C::TM_DP, kend, s, p);
+        tc_fence_before();
+        mbar_arrive(&b.s_free);
+        if (active) {
+          // dS = P o (dP - delta), P = 2^(s*sl2 - lse2); keys >= N contribute 0
 #pragma unroll
-        for (int k = 0; k < DQK; k += 16)
-          mma_bf16(dS, desc_pos_by_ch<kNCHW>(tQ, k), desc_pos_by_ch<kNCHW>(tK, k), idSP,
-                   k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < DV; k += 16)
-          mma_bf16(dP, desc_pos_by_ch<kNCHW>(tDO, k), desc_pos_by_ch<kNCHW>(tV, k), idSP,
-                   k > 0 ? 1u : 0u);
-        mma_commit(&s_full[j & 1]);
-        if (j >= 1 && !issue_dq(j - 1)) ok = false;
-      }
-      if (ok) issue_dq(nkv - 1);
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
-    }
-  } else {
-    const int r = threadIdx.x;
-    const int q = q0 + r;
-    const bool live = q < N;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    // delta of this row, and the row's lse in the log2 domain
-    float D = 0.f, lse2 = 0.f;
-    if (live) {
-      if (kNCHW) {
-        const __nv_bfloat16* o = args.o + (long long)och0 * N + q;
-        const __nv_bfloat16* g = args.dO + (long long)och0 * N + q;
-#pragma unroll 8
-        for (int c = 0; c < DV; ++c) D = fmaf(bf(o[(long long)c * N]), bf(g[(long long)c * N]), D);
-      } else {
-        const uint4* o = reinterpret_cast<const uint4*>(args.o + ((long long)bh * N + q) * DV);
-        const uint4* g = reinterpret_cast<const uint4*>(args.dO + ((long long)bh * N + q) * DV);
-#pragma unroll
-        for (int c = 0; c < DV / 8; ++c) {
-          const uint4 ov = o[c], gv = g[c];
-          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
-            D = fmaf(of.x, gf.x, D);
-            D = fmaf(of.y, gf.y, D);
+          for (int c = 0; c < 64; c += 2) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, -lse2));
+            float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 1]), sl2, -lse2));
+            if (valid < C::BN) {
+              p0 = c < valid ? p0 : 0.f;
+              p1 = c + 1 < valid ? p1 : 0.f;
+            }
+            s[c / 2] = pack_bf16x2(p0 * (__uint_as_float(p[c]) - D), p1 * (__uint_as_float(p[c + 1]) - D));
           }
         }
+        if (k >= 2 && !mbar_wait(&b.ds_free[k & 1], ((k >> 1) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (active) store_row64(sbase + C::OFF_DS + (k & 1) * C::DS_BYTES, r, kend, s);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&b.ds_full[k & 1]);
       }
-      args.delta[(long long)bh * N + q] = D;
-      lse2 = args.lse[(long long)bh * N + q] * 1.4426950408889634f;
-    }
-    const float sl2 = args.scale_log2;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      if (j >= 2 && !mbar_wait(&ds_free[sb], ((j - 2) >> 1) & 1, abort)) {
+      if (!ok) break;
+      const int klast = u * nkv + nkv - 1;
+      if (!mbar_wait(&b.ds_free[klast & 1], (klast >> 1) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int valid = min(C::BN, N - j * C::BN);
-      const uint32_t drow = sbase + C::OFF_DS + sb * C::DS_BYTES;
+      if (active) {
+        float acc[32];
 #pragma unroll
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        float s[32], dp[32];
-        tmem_load32(tmem + lane_base + sb * 128 + c0, s);
-        tmem_load32(tmem + lane_base + sb * 128 + 64 + c0, dp);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float g[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = ch * 8 + e;
-            const float p = (c0 + c < valid) ? fast_exp2(fmaf(s[c], sl2, -lse2)) : 0.f;
-            g[e] = p * (dp[c] - D);
-          }
-          st_shared_v4(drow + swizzled_offset(r, (c0 >> 3) + ch, 128), pack_bf16x2(g[0], g[1]),
-                       pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ds_full[sb]);
-    }
-    if (ok && mbar_wait(mma_done, 0, abort)) {
-      tc_fence_after();
-      float acc[32];
-#pragma unroll
-      for (int c = 0; c < DQK; c += 32) {
-        tmem_load32(tmem + lane_base + C::TM_DQ + c, acc);
-        if (live) {
-          if (kNCHW) {
-            __nv_bfloat16* dst = args.dq + ((long long)ch0 + c) * N + q;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * args.scale);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(args.dq + ((long long)bh * N + q) * DQK + c);
+        for (int c = 0; c < DQK; c += 32) {
+          tmem_load32(tmem + lane_base + C::TM_DQ + c, acc);
+          if (live) {
             const float sc = args.scale;
+            if (kNCHW) {
+              __nv_bfloat16* dst = args.dq + ((long long)qkv_row(bh) + c) * N + q;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              dst[e / 8] = make_uint4(pack_bf16x2(acc[e] * sc, acc[e + 1] * sc),
-                                      pack_bf16x2(acc[e + 2] * sc, acc[e + 3] * sc),
-                                      pack_bf16x2(acc[e + 4] * sc, acc[e + 5] * sc),
-                                      pack_bf16x2(acc[e + 6] * sc, acc[e + 7] * sc));
+              for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(args.dq + ((long long)bh * N + q) * DQK + c);
+#pragma unroll
+              for (int e = 0; e < 32; e += 8)
+                dst[e / 8] = make_uint4(pack_bf16x2(acc[e] * sc, acc[e + 1] * sc),
+                                        pack_bf16x2(acc[e + 2] * sc, acc[e + 3] * sc),
+                                        pack_bf16x2(acc[e + 4] * sc, acc[e + 5] * sc),
+                                        pack_bf16x2(acc[e + 6] * sc, acc[e + 7] * sc));
+            }
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&b.dq_free);
     }
   }
 
@@ -277,67 +379,74 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ====================================================================== dK / dV
-template <int DQK, int DV, bool kNCHW>
+template <int DQK, int DV, bool kNCHW, int KVBUF, int ST, int CPS>
 struct DkvCfg {
-  static constexpr int BM = 128 /* keys */, BQ = 64 /* queries per tile */, STAGES = 2;
-  static constexpr int kThreads = 192;
+  static constexpr int BM = 128 /* keys */, BQ = 64 /* queries per tile */, kThreads = 192;
+  static constexpr int STAGES = ST;
+  static_assert(KVBUF >= 1 && KVBUF <= 2 && ST >= 2 && ST <= 4, "buffering");
   static constexpr uint32_t K_BYTES = BM * DQK * 2, V_BYTES = BM * DV * 2;
   static constexpr uint32_t Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
-  static constexpr uint32_t STAT_BYTES = 1024;  // lse2[64] + delta[64], padded
+  static constexpr uint32_t STAT_BYTES = 2 * BQ * 4;  // lse2[64], delta[64]
   static constexpr uint32_t PT_BYTES = BM * BQ * 2;
-  static constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + K_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_V + V_BYTES;
-  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * Q_BYTES;
-  static constexpr uint32_t OFF_STAT = OFF_DO + STAGES * DO_BYTES;
-  static constexpr uint32_t OFF_PT = OFF_STAT + STAGES * STAT_BYTES;
-  static constexpr uint32_t OFF_DST = OFF_PT + 2 * PT_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_DST + 2 * PT_BYTES;
-  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM: S^T[b] at 128 b, dP^T[b] at 128 b + 64, dV at 256, dK at 256 + DV
-  static constexpr uint32_t TM_DV = 256, TM_DK = 256 + DV;
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(TM_DK + DQK <= TMEM_COLS, "tensor memory");
+  static constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + KVBUF * K_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_V + KVBUF * V_BYTES;
+  static constexpr uint32_t OFF_DO = OFF_Q + ST * Q_BYTES;
+  static constexpr uint32_t OFF_PT = OFF_DO + ST * DO_BYTES;
+  static constexpr uint32_t OFF_DST = OFF_PT + PT_BYTES;
+  static constexpr uint32_t OFF_STAT = OFF_DST + PT_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_STAT + ST * STAT_BYTES;
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+  // TMEM: S^T at 0, dP^T at 64, dV at 128, dK after dV
+  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 128 + DV;
+  static constexpr uint32_t TMEM_COLS = TM_DK + DQK <= 256 ? 256 : 512;
+  static_assert(SMEM_BYTES <= 227 * 1024 && (CPS == 1 || SMEM_BYTES <= 113 * 1024), "shared memory");
+  static_assert(CPS == 1 || TMEM_COLS <= 256, "tensor memory");
 };
 
-template <int DQK, int DV, bool kNCHW>
-__global__ void __launch_bounds__(192, 1)
+struct DkvBars {
+  uint64_t kv_full[2], kv_empty[2], q_full[4], q_empty[4];
+  uint64_t s_full, s_free, p_full, pds_free, acc_free, mma_done;
+};
+
+template <int DQK, int DV, bool kNCHW, int KVBUF, int ST, int CPS>
+__global__ void __launch_bounds__(192, CPS)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmDO, const BwdArgs args) {
-  using C = DkvCfg<DQK, DV, kNCHW>;
+  using C = DkvCfg<DQK, DV, kNCHW, KVBUF, ST, CPS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t sbase = smem_addr(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;    // [2]
-  uint64_t* q_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* pds_free = bars + 9;  // [2]
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  DkvBars& b = *reinterpret_cast<DkvBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&b + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y, k0 = blockIdx.x * C::BM, N = args.N;
+  const int N = args.N;
   const int nq = (N + C::BQ - 1) / C::BQ;
-  const int b = bh / args.nh, hd = bh % args.nh;
-  const int ch0 = kNCHW ? b * args.qkv_ch + hd * 4 * DQK : 0;
-  const int och0 = kNCHW ? b * args.out_ch + hd * DV : 0;
+  const int nkt = (N + C::BM - 1) / C::BM;
+  const int T = args.BH * nkt;
+  const int nunits = unit_count(blockIdx.x, gridDim.x, T);
+  auto unit_of = [&](int u) { return (int)blockIdx.x + u * (int)gridDim.x; };
+  auto qkv_row = [&](int bh) { return kNCHW ? (bh / args.nh) * args.qkv_ch + (bh % args.nh) * 4 * DQK : 0; };
+  auto out_row = [&](int bh) { return kNCHW ? (bh / args.nh) * args.out_ch + (bh % args.nh) * DV : 0; };
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(q_full + i, 1 + 32);
-      mbar_init(q_empty + i, 1);
-      mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
-      mbar_init(pds_free + i, 1);
+      mbar_init(&b.kv_full[i], 1);
+      mbar_init(&b.kv_empty[i], 1);
     }
-    mbar_init(mma_done, 1);
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&b.q_full[i], 1 + 32);
+      mbar_init(&b.q_empty[i], 1);
+    }
+    mbar_init(&b.s_full, 1);
+    mbar_init(&b.s_free, 128);
+    mbar_init(&b.p_full, 128);
+    mbar_init(&b.pds_free, 1);
+    mbar_init(&b.acc_free, 128);
+    mbar_init(&b.mma_done, 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -351,181 +460,240 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
-    // producer: K/V once; per query tile Q, dO by TMA and lse / delta by plain loads
-    if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, C::K_BYTES + C::V_BYTES);
-      load_tile<kNCHW, DQK>(smem + C::OFF_K, &tmK, kv_full, C::BM, k0, bh, ch0 + DQK);
-      load_tile<kNCHW, DV>(smem + C::OFF_V, &tmV, kv_full, C::BM, k0, bh, ch0 + 2 * DQK);
-    }
-    int issued = 0;
-    for (int i = 0; i < nq; ++i) {
-      const int st = i % C::STAGES;
-      if (i >= C::STAGES && !mbar_wait(&q_empty[st], ((i / C::STAGES) - 1) & 1, abort)) break;
+    // producer: K/V per unit by TMA; per query tile Q, dO by TMA and lse / delta by
+    // plain loads of all 32 lanes (33 arrivals complete a stage)
+    bool ok = true;
+    int kv_issued = 0, q_issued = 0;
+    auto issue_kv = [&](int u) -> bool {
+      const int t = unit_of(u), bh = t / nkt, k0 = (t % nkt) * C::BM;
+      const int kb = u % KVBUF;
+      if (u >= KVBUF && !mbar_wait(&b.kv_empty[kb], ((u / KVBUF) - 1) & 1, abort)) return false;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&q_full[st], C::Q_BYTES + C::DO_BYTES);
-        load_tile<kNCHW, DQK>(smem + C::OFF_Q + st * C::Q_BYTES, &tmQ, &q_full[st], C::BQ,
-                              i * C::BQ, bh, ch0);
-        load_tile<kNCHW, DV>(smem + C::OFF_DO + st * C::DO_BYTES, &tmDO, &q_full[st], C::BQ,
-                             i * C::BQ, bh, och0);
+        mbar_arrive_expect_tx(&b.kv_full[kb], C::K_BYTES + C::V_BYTES);
+        load_tile<kNCHW, DQK>(smem + C::OFF_K + kb * C::K_BYTES, &tmK, &b.kv_full[kb], C::BM, k0, bh,
+                              qkv_row(bh) + DQK);
+        load_tile<kNCHW, DV>(smem + C::OFF_V + kb * C::V_BYTES, &tmV, &b.kv_full[kb], C::BM, k0, bh,
+                             qkv_row(bh) + 2 * DQK);
       }
-      float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
+      kv_issued = u + 1;
+      return true;
+    };
+    if (nunits > 0) ok = issue_kv(0);
+    for (int u = 0; ok && u < nunits; ++u) {
+      const int bh = unit_of(u) / nkt;
+      for (int i = 0; ok && i < nq; ++i) {
+        const int g = u * nq + i, st = g % C::STAGES;
+        if (g >= C::STAGES && !mbar_wait(&b.q_empty[st], ((g / C::STAGES) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&b.q_full[st], C::Q_BYTES + C::DO_BYTES);
+          load_tile<kNCHW, DQK>(smem + C::OFF_Q + st * C::Q_BYTES, &tmQ, &b.q_full[st], C::BQ,
+                                i * C::BQ, bh, qkv_row(bh));
+          load_tile<kNCHW, DV>(smem + C::OFF_DO + st * C::DO_BYTES, &tmDO, &b.q_full[st], C::BQ,
+                               i * C::BQ, bh, out_row(bh));
+        }
+        float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
 #pragma unroll
-      for (int e = lane; e < C::BQ; e += 32) {
-        const int q = i * C::BQ + e;
-        const bool in = q < N;
-        stat[e] = in ? args.lse[(long long)bh * N + q] * 1.4426950408889634f : INFINITY;
-        stat[C::BQ + e] = in ? args.delta[(long long)bh * N + q] : 0.f;
+        for (int e = lane; e < C::BQ; e += 32) {
+          const int q = i * C::BQ + e;
+          const bool in = q < N;
+          stat[e] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
+          stat[C::BQ + e] = in ? args.delta[(long long)bh * N + q] : 0.f;
+        }
+        mbar_arrive(&b.q_full[st]);
+        q_issued = g + 1;
+        if (KVBUF == 2 && i == 0 && u + 1 < nunits) ok = issue_kv(u + 1);
+        if (KVBUF == 1 && i == nq - 1 && u + 1 < nunits) ok = issue_kv(u + 1);
       }
-      mbar_arrive(&q_full[st]);
-      issued = i + 1;
     }
     if (lane == 0 && *abort) {
-      drain_wait(kv_full, 0);
-      for (int i = (issued > C::STAGES ? issued - C::STAGES : 0); i < issued; ++i)
-        drain_wait(&q_full[i % C::STAGES], (i / C::STAGES) & 1);
+      for (int u = max(0, kv_issued - KVBUF); u < kv_issued; ++u)
+        drain_wait(&b.kv_full[u % KVBUF], (u / KVBUF) & 1);
+      for (int g = max(0, q_issued - C::STAGES); g < q_issued; ++g)
+        drain_wait(&b.q_full[g % C::STAGES], (g / C::STAGES) & 1);
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      const SmemTile tK = tile_view<kNCHW, DQK>(sbase + C::OFF_K, C::BM);
-      const SmemTile tV = tile_view<kNCHW, DV>(sbase + C::OFF_V, C::BM);
-      const uint32_t idSP = idesc_bf16_f32(128, C::BQ, kNCHW, kNCHW);
+      const uint64_t dK0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_K, C::BM), 0);
+      const uint64_t dV0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DV>(sbase + C::OFF_V, C::BM), 0);
+      const uint64_t dQ0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_Q, C::BQ), 0);
+      const uint64_t dDO0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DV>(sbase + C::OFF_DO, C::BQ), 0);
+      const uint64_t dQb0 = desc_ch_by_pos<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::OFF_Q, C::BQ), 0);
+      const uint64_t dDOb0 = desc_ch_by_pos<kNCHW>(tile_view<kNCHW, DV>(sbase + C::OFF_DO, C::BQ), 0);
+      const uint64_t dPT = desc_kmajor(SmemTile{sbase + C::OFF_PT, 128, C::BM}, 0);
+      const uint64_t dDST = desc_kmajor(SmemTile{sbase + C::OFF_DST, 128, C::BM}, 0);
+      constexpr uint64_t kStepQK = kstep_pos_by_ch<kNCHW, DQK>(), kStepV = kstep_pos_by_ch<kNCHW, DV>();
+      constexpr uint64_t kStepQb = kstep_ch_by_pos<kNCHW, DQK>(), kStepDOb = kstep_ch_by_pos<kNCHW, DV>();
+      constexpr uint64_t kStepT = 32 >> 4;
+      const uint32_t idSP_full = idesc_bf16_f32(128, C::BQ, kNCHW, kNCHW);
       const uint32_t idDV = idesc_bf16_f32(128, DV, false, !kNCHW);
       const uint32_t idDK = idesc_bf16_f32(128, DQK, false, !kNCHW);
-      auto issue_grad = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort)) return false;
+      auto issue_s = [&](int u, int i) -> bool {
+        const int g = u * nq + i;
+        if ((i == 0 && !mbar_wait(&b.kv_full[u % KVBUF], (u / KVBUF) & 1, abort)) ||
+            !mbar_wait(&b.q_full[g % C::STAGES], (g / C::STAGES) & 1, abort) ||
+            (g >= 1 && !mbar_wait(&b.s_free, (g - 1) & 1, abort)))
+          return false;
         tc_fence_after();
-        const int st = i % C::STAGES;
-        const SmemTile tQ = tile_view<kNCHW, DQK>(sbase + C::OFF_Q + st * C::Q_BYTES, C::BQ);
-        const SmemTile tDO = tile_view<kNCHW, DV>(sbase + C::OFF_DO + st * C::DO_BYTES, C::BQ);
-        const SmemTile tPt{sbase + C::OFF_PT + (i & 1) * C::PT_BYTES, 128, C::BM};
-        const SmemTile tDSt{sbase + C::OFF_DST + (i & 1) * C::PT_BYTES, 128, C::BM};
+        const uint64_t dK = dK0 + (uint64_t)((u % KVBUF) * C::K_BYTES >> 4);
+        const uint64_t dV = dV0 + (uint64_t)((u % KVBUF) * C::V_BYTES >> 4);
+        const uint64_t dQ = dQ0 + (uint64_t)((g % C::STAGES) * C::Q_BYTES >> 4);
+        const uint64_t dDO = dDO0 + (uint64_t)((g % C::STAGES) * C::DO_BYTES >> 4);
         const int valid = min(C::BQ, N - i * C::BQ);
-        const int kend = (valid + 15) & ~15;
-        for (int k = 0; k < kend; k += 16) {
-          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
-          mma_bf16(tmem + C::TM_DV, desc_kmajor(tPt, k), desc_ch_by_pos<kNCHW>(tDO, k), idDV, acc);
-          mma_bf16(tmem + C::TM_DK, desc_kmajor(tDSt, k), desc_ch_by_pos<kNCHW>(tQ, k), idDK, acc);
-        }
-        mma_commit(&pds_free[i & 1]);
-        mma_commit(&q_empty[st]);
+        const uint32_t idSP =
+            valid == C::BQ ? idSP_full : idesc_bf16_f32(128, (valid + 15) & ~15, kNCHW, kNCHW);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_bf16(tmem + C::TM_S, dK + kk * kStepQK, dQ + kk * kStepQK, idSP, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_bf16(tmem + C::TM_DP, dV + kk * kStepV, dDO + kk * kStepV, idSP, kk > 0 ? 1u : 0u);
+        mma_commit(&b.s_full);
         return true;
       };
-      bool ok = mbar_wait(kv_full, 0, abort);
-      for (int i = 0; ok && i < nq; ++i) {
-        const int st = i % C::STAGES;
-        if (!mbar_wait(&q_full[st], (i / C::STAGES) & 1, abort)) {
+      auto issue_grad = [&](int u, int i) -> bool {
+        const int g = u * nq + i;
+        if (!mbar_wait(&b.p_full, g & 1, abort) ||
+            (i == 0 && u >= 1 && !mbar_wait(&b.acc_free, (u - 1) & 1, abort)))
+          return false;
+        tc_fence_after();
+        const uint64_t dQb = dQb0 + (uint64_t)((g % C::STAGES) * C::Q_BYTES >> 4);
+        const uint64_t dDOb = dDOb0 + (uint64_t)((g % C::STAGES) * C::DO_BYTES >> 4);
+        const int valid = min(C::BQ, N - i * C::BQ);
+        for (int kk = 0; kk * 16 < valid; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16(tmem + C::TM_DV, dPT + kk * kStepT, dDOb + kk * kStepDOb, idDV, acc);
+          mma_bf16(tmem + C::TM_DK, dDST + kk * kStepT, dQb + kk * kStepQb, idDK, acc);
+        }
+        mma_commit(&b.pds_free);
+        mma_commit(&b.q_empty[g % C::STAGES]);
+        if (i == nq - 1) mma_commit(&b.kv_empty[u % KVBUF]);
+        return true;
+      };
+      bool ok = true;
+      for (int u = 0; ok && u < nunits; ++u) {
+        ok = issue_s(u, 0);
+        for (int i = 0; ok && i < nq; ++i) {
+          if (i + 1 < nq) ok = issue_s(u, i + 1);
+          if (ok) ok = issue_grad(u, i);
+        }
+      }
+      mma_commit(&b.mma_done);
+      drain_wait(&b.mma_done, 0);
+    }
+  } else {
+    const int r = threadIdx.x;  // key row = TMEM lane
+    const int wq = warp;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float sl2 = args.scale_log2;
+    bool ok = true;
+    for (int u = 0; ok && u < nunits; ++u) {
+      const int t = unit_of(u), bh = t / nkt, k0 = (t % nkt) * C::BM;
+      const bool active = wq * 32 < N - k0;
+      const int key = k0 + r;
+      for (int i = 0; i < nq; ++i) {
+        const int g = u * nq + i, st = g % C::STAGES;
+        const int valid = min(C::BQ, N - i * C::BQ);
+        const int kend = (valid + 15) & ~15;
+        if (!mbar_wait(&b.s_full, g & 1, abort) ||
+            !mbar_wait(&b.q_full[st], (g / C::STAGES) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const SmemTile tQ = tile_view<kNCHW, DQK>(sbase + C::OFF_Q + st * C::Q_BYTES, C::BQ);
-        const SmemTile tDO = tile_view<kNCHW, DV>(sbase + C::OFF_DO + st * C::DO_BYTES, C::BQ);
-        const uint32_t dS = tmem + (i & 1) * 128, dP = dS + 64;
+        uint32_t s[64], p[64];
+        if (active) load_sp_rows(tmem + lane_base + C::TM_S, tmem + lane_base + C::TM_DP, kend, s, p);
+        tc_fence_before();
+        mbar_arrive(&b.s_free);
+        if (active) {
+          const float4* st4 = reinterpret_cast<const float4*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
+          // P^T = 2^(s*sl2 - lse2[q]) (lse2 = +inf for queries >= N gives 0),
+          // dS^T = P^T (dP^T - delta[q])
 #pragma unroll
-        for (int k = 0; k < DQK; k += 16)
-          mma_bf16(dS, desc_pos_by_ch<kNCHW>(tK, k), desc_pos_by_ch<kNCHW>(tQ, k), idSP,
-                   k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < DV; k += 16)
-          mma_bf16(dP, desc_pos_by_ch<kNCHW>(tV, k), desc_pos_by_ch<kNCHW>(tDO, k), idSP,
-                   k > 0 ? 1u : 0u);
-        mma_commit(&s_full[i & 1]);
-        if (i >= 1 && !issue_grad(i - 1)) ok = false;
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = st4[c / 4], d4 = st4[C::BQ / 4 + c / 4];
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, -l4.x));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 1]), sl2, -l4.y));
+            const float p2 = fast_exp2(fmaf(__uint_as_float(s[c + 2]), sl2, -l4.z));
+            const float p3 = fast_exp2(fmaf(__uint_as_float(s[c + 3]), sl2, -l4.w));
+            s[c / 2] = pack_bf16x2(p0, p1);
+            s[c / 2 + 1] = pack_bf16x2(p2, p3);
+            p[c / 2] = pack_bf16x2(p0 * (__uint_as_float(p[c]) - d4.x),
+                                   p1 * (__uint_as_float(p[c + 1]) - d4.y));
+            p[c / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(p[c + 2]) - d4.z),
+                                       p3 * (__uint_as_float(p[c + 3]) - d4.w));
+          }
+        }
+        if (g >= 1 && !mbar_wait(&b.pds_free, (g - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          store_row64(sbase + C::OFF_PT, r, kend, s);
+          store_row64(sbase + C::OFF_DST, r, kend, p);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&b.p_full);
       }
-      if (ok) issue_grad(nq - 1);
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
-    }
-  } else {
-    const int r = threadIdx.x;  // key row = TMEM lane
-    const int key = k0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float sl2 = args.scale_log2;
-    bool ok = true;
-    for (int i = 0; i < nq; ++i) {
-      const int sb = i & 1, st = i % C::STAGES;
-      if (!mbar_wait(&s_full[sb], (i >> 1) & 1, abort) ||
-          !mbar_wait(&q_full[st], (i / C::STAGES) & 1, abort) ||
-          (i >= 2 && !mbar_wait(&pds_free[sb], ((i - 2) >> 1) & 1, abort))) {
+      if (!ok) break;
+      const int glast = u * nq + nq - 1;
+      if (!mbar_wait(&b.pds_free, glast & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
-      const uint32_t prow = sbase + C::OFF_PT + sb * C::PT_BYTES;
-      const uint32_t drow = sbase + C::OFF_DST + sb * C::PT_BYTES;
+      if (active) {
+        const bool live = key < N;
+        float acc[32];
 #pragma unroll
-      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
-        float s[32], dp[32];
-        tmem_load32(tmem + lane_base + sb * 128 + c0, s);
-        tmem_load32(tmem + lane_base + sb * 128 + 64 + c0, dp);
+        for (int c = 0; c < DV; c += 32) {
+          tmem_load32(tmem + lane_base + C::TM_DV + c, acc);
+          if (live) {
+            if (kNCHW) {
+              __nv_bfloat16* dst = args.dv + ((long long)qkv_row(bh) + 2 * DQK + c) * N + key;
+              const __nv_bfloat16* res =
+                  args.dvres ? args.dvres + ((long long)out_row(bh) + c) * N + key : nullptr;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float p[8], g[8];
+              for (int e = 0; e < 32; ++e) {
+                float x = acc[e];
+                if (res) x += bf(res[(long long)e * N]);
+                dst[(long long)e * N] = __float2bfloat16_rn(x);
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(args.dv + ((long long)bh * N + key) * DV + c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = ch * 8 + e;
-            p[e] = fast_exp2(fmaf(s[c], sl2, -stat[c0 + c]));  // lse2 = +inf past N
-            g[e] = p[e] * (dp[c] - stat[C::BQ + c0 + c]);
-          }
-          const uint32_t off = swizzled_offset(r, (c0 >> 3) + ch, 128);
-          st_shared_v4(prow + off, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                       pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
-          st_shared_v4(drow + off, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                       pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[sb]);
-    }
-    if (ok && mbar_wait(mma_done, 0, abort)) {
-      tc_fence_after();
-      const bool live = key < N;
-      float acc[32];
-#pragma unroll
-      for (int c = 0; c < DV; c += 32) {
-        tmem_load32(tmem + lane_base + C::TM_DV + c, acc);
-        if (live) {
-          if (kNCHW) {
-            __nv_bfloat16* dst = args.dv + ((long long)ch0 + 2 * DQK + c) * N + key;
-            const __nv_bfloat16* res =
-                args.dvres ? args.dvres + ((long long)och0 + c) * N + key : nullptr;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float x = acc[e];
-              if (res) x += bf(res[(long long)e * N]);
-              dst[(long long)e * N] = __float2bfloat16_rn(x);
+              for (int e = 0; e < 32; e += 8)
+                dst[e / 8] = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
+                                        pack_bf16x2(acc[e + 4], acc[e + 5]), pack_bf16x2(acc[e + 6], acc[e + 7]));
             }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(args.dv + ((long long)bh * N + key) * DV + c);
+          }
+        }
+        const float sc = args.scale;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              dst[e / 8] = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
-                                      pack_bf16x2(acc[e + 4], acc[e + 5]), pack_bf16x2(acc[e + 6], acc[e + 7]));
+        for (int c = 0; c < DQK; c += 32) {
+          tmem_load32(tmem + lane_base + C::TM_DK + c, acc);
+          if (live) {
+            if (kNCHW) {
+              __nv_bfloat16* dst = args.dk + ((long long)qkv_row(bh) + DQK + c) * N + key;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(args.dk + ((long long)bh * N + key) * DQK + c);
+#pragma unroll
+              for (int e = 0; e < 32; e += 8)
+                dst[e / 8] = make_uint4(pack_bf16x2(acc[e] * sc, acc[e + 1] * sc),
+                                        pack_bf16x2(acc[e + 2] * sc, acc[e + 3] * sc),
+                                        pack_bf16x2(acc[e + 4] * sc, acc[e + 5] * sc),
+                                        pack_bf16x2(acc[e + 6] * sc, acc[e + 7] * sc));
+            }
           }
         }
       }
-      const float sc = args.scale;
-#pragma unroll
-      for (int c = 0; c < DQK; c += 32) {
-        tmem_load32(tmem + lane_base + C::TM_DK + c, acc);
-        if (live) {
-          if (kNCHW) {
-            __nv_bfloat16* dst = args.dk + ((long long)ch0 + DQK + c) * N + key;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(args.dk + ((long long)bh * N + key) * DQK + c);
-#pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              dst[e / 8] = make_uint4(pack_bf16x2(acc[e] * sc, acc[e + 1] * sc),
-                                      pack_bf16x2(acc[e + 2] * sc, acc[e + 3] * sc),
-                                      pack_bf16x2(acc[e + 4] * sc, acc[e + 5] * sc),
-                                      pack_bf16x2(acc[e + 6] * sc, acc[e + 7] * sc));
-          }
-        }
-      }
+      tc_fence_before();
+      mbar_arrive(&b.acc_free);
     }
   }
 
@@ -537,16 +705,33 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <typename Cfg, typename K>
+template <typename Cfg, int CPS, typename K>
 cudaError_t launch(K kern, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                   const CUtensorMap& mDO, const BwdArgs& a, int BH, int tile,
+                   const CUtensorMap& mDO, const BwdArgs& a, int rows_per_unit,
                    cudaStream_t st) {
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
-  dim3 grid((a.N + tile - 1) / tile, BH);
-  kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQ, mK, mV, mDO, a);
+  const long long units = (long long)a.BH * ((a.N + rows_per_unit - 1) / rows_per_unit);
+  const long long ctas = std::min<long long>((long long)CPS * device_sm_count(), units);
+  kern<<<(unsigned)ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQ, mK, mV, mDO, a);
   return cudaGetLastError();
+}
+
+// <DQK, DV, layout, Q or K/V buffers, stages, CTAs per SM>
+template <int DQK, int DV, bool kNCHW, int QB, int ST, int CPS>
+cudaError_t run_dq(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                   const CUtensorMap& mDO, const BwdArgs& a, cudaStream_t st) {
+  using Cfg = DqCfg<DQK, DV, kNCHW, QB, ST, CPS>;
+  return launch<Cfg, CPS>(attn_bwd_dq_kernel<DQK, DV, kNCHW, QB, ST, CPS>, mQ, mK, mV, mDO, a,
+                          Cfg::BM, st);
+}
+template <int DQK, int DV, bool kNCHW, int KB, int ST, int CPS>
+cudaError_t run_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                     const CUtensorMap& mDO, const BwdArgs& a, cudaStream_t st) {
+  using Cfg = DkvCfg<DQK, DV, kNCHW, KB, ST, CPS>;
+  return launch<Cfg, CPS>(attn_bwd_dkdv_kernel<DQK, DV, kNCHW, KB, ST, CPS>, mQ, mK, mV, mDO, a,
+                          Cfg::BM, st);
 }
 
 }  // namespace
@@ -554,33 +739,33 @@ cudaError_t launch(K kern, const CUtensorMap& mQ, const CUtensorMap& mK, const C
 cudaError_t launch_fa2_bwd_dq(const CUtensorMap& mQ, const CUtensorMap& mK,
                               const CUtensorMap& mV, const CUtensorMap& mDO, const BwdArgs& a,
                               int BH, int d, cudaStream_t st) {
-  if (d == 32)
-    return launch<DqCfg<32, 32, false>>(attn_bwd_dq_kernel<32, 32, false>, mQ, mK, mV, mDO, a, BH, 128, st);
-  return launch<DqCfg<64, 64, false>>(attn_bwd_dq_kernel<64, 64, false>, mQ, mK, mV, mDO, a, BH, 128, st);
+  (void)BH;
+  if (d == 32) return run_dq<32, 32, false, 2, 4, 2>(mQ, mK, mV, mDO, a, st);
+  return run_dq<64, 64, false, 1, 2, 2>(mQ, mK, mV, mDO, a, st);
 }
 
 cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
                                 const CUtensorMap& mV, const CUtensorMap& mDO,
                                 const BwdArgs& a, int BH, int d, cudaStream_t st) {
-  if (d == 32)
-    return launch<DkvCfg<32, 32, false>>(attn_bwd_dkdv_kernel<32, 32, false>, mQ, mK, mV, mDO, a, BH, 128, st);
-  return launch<DkvCfg<64, 64, false>>(attn_bwd_dkdv_kernel<64, 64, false>, mQ, mK, mV, mDO, a, BH, 128, st);
+  (void)BH;
+  if (d == 32) return run_dkdv<32, 32, false, 2, 3, 2>(mQ, mK, mV, mDO, a, st);
+  return run_dkdv<64, 64, false, 1, 2, 2>(mQ, mK, mV, mDO, a, st);
 }
 
 cudaError_t launch_psa_bwd_dq(const CUtensorMap& mQK, const CUtensorMap& mV,
                               const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                               cudaStream_t st) {
-  if (KD == 32)
-    return launch<DqCfg<32, 64, true>>(attn_bwd_dq_kernel<32, 64, true>, mQK, mQK, mV, mDO, a, BH, 128, st);
-  return launch<DqCfg<64, 128, true>>(attn_bwd_dq_kernel<64, 128, true>, mQK, mQK, mV, mDO, a, BH, 128, st);
+  (void)BH;
+  if (KD == 32) return run_dq<32, 64, true, 1, 4, 2>(mQK, mQK, mV, mDO, a, st);
+  return run_dq<64, 128, true, 2, 3, 1>(mQK, mQK, mV, mDO, a, st);
 }
 
 cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st) {
-  if (KD == 32)
-    return launch<DkvCfg<32, 64, true>>(attn_bwd_dkdv_kernel<32, 64, true>, mQK, mQK, mV, mDO, a, BH, 128, st);
-  return launch<DkvCfg<64, 128, true>>(attn_bwd_dkdv_kernel<64, 128, true>, mQK, mQK, mV, mDO, a, BH, 128, st);
+  (void)BH;
+  if (KD == 32) return run_dkdv<32, 64, true, 2, 2, 2>(mQK, mQK, mV, mDO, a, st);
+  return run_dkdv<64, 128, true, 2, 3, 1>(mQK, mQK, mV, mDO, a, st);
 }
 
 }  // namespace psa
