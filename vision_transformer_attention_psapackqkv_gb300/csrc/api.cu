@@ -324,12 +324,14 @@ psa_status_t validate_bwd(const void* qkv, const void* dout, const float* lse, c
 psa_status_t make_bwd(const void* qkv, const void* dout, const float* lse, const void* dqkv,
                       const float* delta, const void* dvres, const void* out,
                       const psa_shape_t& s, float scale, CUtensorMap* mqk, CUtensorMap* mv,
-                      CUtensorMap* mdo, BwdArgs* a) {
+                      CUtensorMap* mdo, CUtensorMap* mo, BwdArgs* a) {
   const int N = s.H * s.W;
   const int nh = s.num_heads, KD = s.key_dim;
   const long long rows = (long long)s.B * nh * 4 * KD;
+  const long long out_rows = (long long)s.B * nh * 2 * KD;
   if (!map_nchw(mqk, qkv, rows, N, KD) || !map_nchw(mv, qkv, rows, N, 2 * KD) ||
-      !map_nchw(mdo, dout, (long long)s.B * nh * 2 * KD, N, 2 * KD))
+      !map_nchw(mdo, dout, out_rows, N, 2 * KD) ||
+      (out && !map_nchw(mo, out, out_rows, N, 2 * KD)))
     return PSA_ERR_CUDA;
   *a = BwdArgs{};
   a->N = N;
@@ -352,12 +354,13 @@ psa_status_t make_bwd(const void* qkv, const void* dout, const float* lse, const
 psa_status_t psa_attention_bwd_dq(const void* qkv, const void* out, const void* dout,
                                   const float* lse, float* delta, void* dqkv, psa_shape_t s,
                                   float scale, cudaStream_t st) {
-  CUtensorMap mqk, mv, mdo;
+  CUtensorMap mqk, mv, mdo, mo;
   BwdArgs a;
   psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
-  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &a);
+  if (e == PSA_OK)
+    e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &mo, &a);
   if (e != PSA_OK) return e;
-  return from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, a, s.B * s.num_heads, s.key_dim, st));
+  return from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, mo, a, s.B * s.num_heads, s.key_dim, st));
 }
 
 psa_status_t psa_attention_bwd_dkdv(const void* qkv, const void* dout, const float* lse,
@@ -366,7 +369,8 @@ psa_status_t psa_attention_bwd_dkdv(const void* qkv, const void* dout, const flo
   CUtensorMap mqk, mv, mdo;
   BwdArgs a;
   psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
-  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk, &mv, &mdo, &a);
+  if (e == PSA_OK)
+    e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk, &mv, &mdo, nullptr, &a);
   if (e != PSA_OK) return e;
   return from_cuda(psa::launch_psa_bwd_dkdv(mqk, mv, mdo, a, s.B * s.num_heads, s.key_dim, st));
 }
@@ -380,15 +384,18 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
   if (ws_bytes < psa_attention_bwd_workspace_size(s)) return PSA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
   // validate both launches completely before issuing either
-  CUtensorMap mqk, mv, mdo, mqk2, mv2, mdo2;
+  CUtensorMap mqk, mv, mdo, mo, mqk2, mv2, mdo2;
   BwdArgs a_dq, a_kv;
   e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
   if (e == PSA_OK) e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
-  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &a_dq);
-  if (e == PSA_OK) e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk2, &mv2, &mdo2, &a_kv);
+  if (e == PSA_OK)
+    e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &mo, &a_dq);
+  if (e == PSA_OK)
+    e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk2, &mv2, &mdo2, nullptr,
+                 &a_kv);
   if (e != PSA_OK) return e;
   const int BH = s.B * s.num_heads;
-  e = from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, a_dq, BH, s.key_dim, st));
+  e = from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, mo, a_dq, BH, s.key_dim, st));
   if (e != PSA_OK) return e;
   return from_cuda(psa::launch_psa_bwd_dkdv(mqk2, mv2, mdo2, a_kv, BH, s.key_dim, st));
 }

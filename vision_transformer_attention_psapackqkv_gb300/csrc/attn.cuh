@@ -69,10 +69,11 @@ cudaError_t launch_fa2_bwd_dq(const CUtensorMap& mQ, const CUtensorMap& mK,
 cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
                                 const CUtensorMap& mV, const CUtensorMap& mDO,
                                 const BwdArgs& a, int BH, int d, cudaStream_t st);
-// NCHW maps: mQK box {64, KD} and mV box {64, 2KD} over QKV; mDO box {64, 2KD} over dOut.
+// NCHW maps: mQK box {64, KD} and mV box {64, 2KD} over QKV; mDO box {64, 2KD} over dOut,
+// mO the same box over Out.
 cudaError_t launch_psa_bwd_dq(const CUtensorMap& mQK, const CUtensorMap& mV,
-                              const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
-                              cudaStream_t st);
+                              const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
+                              int BH, int KD, cudaStream_t st);
 cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st);

@@ -16,14 +16,16 @@
 // back at once, so the next tile's MMAs overlap its exponentials.
 //
 // dQ kernel: unit = (head, 128 query rows); walks 64-key tiles.
-//   prologue (row threads): delta of the row from O and dO, written out for the
-//     dK/dV kernel, which therefore runs after this one.
+//   prologue (row threads): delta of the row from O and dO (NCHW: both tiles
+//     staged by TMA with Q; raw planes: vector global loads), written out for
+//     the dK/dV kernel, which therefore runs after this one.
 //   MMA:  S = Q K_j^T, dP = dO V_j^T (TMEM, 64 columns each); dQ += dS_j K_j
 //         (dS_j bf16 in shared memory, double-buffered).
 // dK/dV kernel: unit = (head, 128 key rows); walks 64-query tiles.
 //   MMA:  S^T = K Q_i^T, dP^T = V dO_i^T; dV += P^T_i dO_i, dK += dS^T_i Q_i.
 //   lse and delta of the 64 query columns come from shared memory, written
-//   there by the producer warp next to each Q / dO stage.
+//   there by the producer warp next to each Q / dO stage (fetched into its
+//   registers one stage ahead).
 // Layouts as in the forward: kNCHW = false uses [BH, N, d] planes, kNCHW = true
 // reads QKV / Out / dOut in NCHW and writes dQKV in NCHW (the adjoints of
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing; the optional
@@ -82,10 +84,14 @@ struct DqCfg {
   static constexpr int BM = 128, BN = 64, kThreads = 192, STAGES = ST;
   static_assert(QBUF >= 1 && QBUF <= 2 && ST >= 2 && ST <= 4, "buffering");
   static constexpr uint32_t Q_BYTES = BM * DQK * 2, DO_BYTES = BM * DV * 2;
+  // NCHW: the O tile is staged by TMA next to dO, so delta comes from shared
+  // memory (strided 2-byte global loads would stall the row threads)
+  static constexpr uint32_t O_BYTES = kNCHW ? BM * DV * 2 : 0;
   static constexpr uint32_t K_BYTES = BN * DQK * 2, V_BYTES = BN * DV * 2;
   static constexpr uint32_t DS_BYTES = BM * BN * 2;
   static constexpr uint32_t OFF_Q = 0, OFF_DO = OFF_Q + QBUF * Q_BYTES;
-  static constexpr uint32_t OFF_K = OFF_DO + QBUF * DO_BYTES;
+  static constexpr uint32_t OFF_O = OFF_DO + QBUF * DO_BYTES;
+  static constexpr uint32_t OFF_K = OFF_O + QBUF * O_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + ST * K_BYTES;
   static constexpr uint32_t OFF_DS = OFF_V + ST * V_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_BYTES;
@@ -107,7 +113,8 @@ __global__ void __launch_bounds__(192, CPS)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmDO, const BwdArgs args) {
+                       const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmO, const BwdArgs args) {
   using C = DqCfg<DQK, DV, kNCHW, QBUF, ST, CPS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -130,7 +137,8 @@ __global__ void __launch_bounds__(192, CPS)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.q_full[i], 1);
-      mbar_init(&b.q_empty[i], 1);
+      // NCHW: the row threads also release the Q stage once delta is read
+      mbar_init(&b.q_empty[i], kNCHW ? 129 : 1);
       mbar_init(&b.ds_full[i], 128);
       mbar_init(&b.ds_free[i], 1);
     }
@@ -163,11 +171,14 @@ __global__ void __launch_bounds__(192, CPS)
         const int t = unit_of(u), bh = t / nqt, q0 = (t % nqt) * C::BM;
         const int qb = u % QBUF;
         if (u >= QBUF && !mbar_wait(&b.q_empty[qb], ((u / QBUF) - 1) & 1, abort)) return false;
-        mbar_arrive_expect_tx(&b.q_full[qb], C::Q_BYTES + C::DO_BYTES);
+        mbar_arrive_expect_tx(&b.q_full[qb], C::Q_BYTES + C::DO_BYTES + C::O_BYTES);
         load_tile<kNCHW, DQK>(smem + C::OFF_Q + qb * C::Q_BYTES, &tmQ, &b.q_full[qb], C::BM, q0, bh,
                               qkv_row(bh));
         load_tile<kNCHW, DV>(smem + C::OFF_DO + qb * C::DO_BYTES, &tmDO, &b.q_full[qb], C::BM, q0,
                              bh, out_row(bh));
+        if (kNCHW)
+          load_tile<kNCHW, DV>(smem + C::OFF_O + qb * C::O_BYTES, &tmO, &b.q_full[qb], C::BM, q0,
+                               bh, out_row(bh));
         q_issued = u + 1;
         return true;
       };
@@ -275,30 +286,44 @@ __global__ void __launch_bounds__(192, CPS)
       const bool live = q < N;
       // delta of this row, and the row's lse in the log2 domain
       float D = 0.f, lse2 = 0.f;
-      if (live) {
-        if (kNCHW) {
-          const __nv_bfloat16* o = args.o + (long long)out_row(bh) * N + q;
-          const __nv_bfloat16* g = args.dO + (long long)out_row(bh) * N + q;
-#pragma unroll 8
-          for (int c = 0; c < DV; ++c) D = fmaf(bf(o[(long long)c * N]), bf(g[(long long)c * N]), D);
-        } else {
-          const uint4* o = reinterpret_cast<const uint4*>(args.o + ((long long)bh * N + q) * DV);
-          const uint4* g = reinterpret_cast<const uint4*>(args.dO + ((long long)bh * N + q) * DV);
+      if (live) lse2 = args.lse[(long long)bh * N + q] * kLog2e;
+      if (kNCHW) {
+        // O and dO tiles: two boxes of 64 positions, one 128-byte swizzled row
+        // per channel; this thread's position is a 2-byte column of every row
+        const int qb = u % QBUF;
+        if (!mbar_wait(&b.q_full[qb], (u / QBUF) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (live) {
+          const unsigned char* to = smem + C::OFF_O + qb * C::O_BYTES + (r >> 6) * (DV * 128);
+          const unsigned char* tg = smem + C::OFF_DO + qb * C::DO_BYTES + (r >> 6) * (DV * 128);
+          const int p = r & 63;
+#pragma unroll 16
+          for (int c = 0; c < DV; ++c) {
+            const uint32_t off = swizzled_offset(c, p >> 3, 128) + (p & 7) * 2;
+            D = fmaf(bf(*reinterpret_cast<const __nv_bfloat16*>(to + off)),
+                     bf(*reinterpret_cast<const __nv_bfloat16*>(tg + off)), D);
+          }
+          args.delta[(long long)bh * N + q] = D;
+        }
+        mbar_arrive(&b.q_empty[qb]);
+      } else if (live) {
+        const uint4* o = reinterpret_cast<const uint4*>(args.o + ((long long)bh * N + q) * DV);
+        const uint4* g = reinterpret_cast<const uint4*>(args.dO + ((long long)bh * N + q) * DV);
 #pragma unroll
-          for (int c = 0; c < DV / 8; ++c) {
-            const uint4 ov = o[c], gv = g[c];
-            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        for (int c = 0; c < DV / 8; ++c) {
+          const uint4 ov = o[c], gv = g[c];
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
-              D = fmaf(of.x, gf.x, D);
-              D = fmaf(of.y, gf.y, D);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+            D = fmaf(of.x, gf.x, D);
+            D = fmaf(of.y, gf.y, D);
           }
         }
         args.delta[(long long)bh * N + q] = D;
-        lse2 = args.lse[(long long)bh * N + q] * kLog2e;
       }
       for (int j = 0; j < nkv; ++j) {
         const int k = u * nkv + j;
@@ -478,7 +503,23 @@ __global__ void __launch_bounds__(192, CPS)
       kv_issued = u + 1;
       return true;
     };
-    if (nunits > 0) ok = issue_kv(0);
+    // lse / delta of a query tile are fetched one stage ahead into registers, so
+    // their global-memory latency overlaps the wait for the next free stage
+    float pl[2], pd[2];
+    auto prefetch_stats = [&](int u, int i) {
+      const int bh = unit_of(u) / nkt;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = i * C::BQ + lane + 32 * h;
+        const bool in = q < N;
+        pl[h] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
+        pd[h] = in ? args.delta[(long long)bh * N + q] : 0.f;
+      }
+    };
+    if (nunits > 0) {
+      prefetch_stats(0, 0);
+      ok = issue_kv(0);
+    }
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = unit_of(u) / nkt;
       for (int i = 0; ok && i < nq; ++i) {
@@ -496,13 +537,15 @@ __global__ void __launch_bounds__(192, CPS)
         }
         float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
 #pragma unroll
-        for (int e = lane; e < C::BQ; e += 32) {
-          const int q = i * C::BQ + e;
-          const bool in = q < N;
-          stat[e] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
-          stat[C::BQ + e] = in ? args.delta[(long long)bh * N + q] : 0.f;
+        for (int h = 0; h < 2; ++h) {
+          stat[lane + 32 * h] = pl[h];
+          stat[C::BQ + lane + 32 * h] = pd[h];
         }
         mbar_arrive(&b.q_full[st]);
+        if (i + 1 < nq)
+          prefetch_stats(u, i + 1);
+        else if (u + 1 < nunits)
+          prefetch_stats(u + 1, 0);
         q_issued = g + 1;
         if (KVBUF == 2 && i == 0 && u + 1 < nunits) ok = issue_kv(u + 1);
         if (KVBUF == 1 && i == nq - 1 && u + 1 < nunits) ok = issue_kv(u + 1);
@@ -705,33 +748,33 @@ __global__ void __launch_bounds__(192, CPS)
   }
 }
 
-template <typename Cfg, int CPS, typename K>
-cudaError_t launch(K kern, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                   const CUtensorMap& mDO, const BwdArgs& a, int rows_per_unit,
-                   cudaStream_t st) {
+template <typename Cfg, int CPS, typename K, typename... Maps>
+cudaError_t launch(K kern, const BwdArgs& a, int rows_per_unit, cudaStream_t st,
+                   const Maps&... maps) {
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   const long long units = (long long)a.BH * ((a.N + rows_per_unit - 1) / rows_per_unit);
   const long long ctas = std::min<long long>((long long)CPS * device_sm_count(), units);
-  kern<<<(unsigned)ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQ, mK, mV, mDO, a);
+  kern<<<(unsigned)ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(maps..., a);
   return cudaGetLastError();
 }
 
 // <DQK, DV, layout, Q or K/V buffers, stages, CTAs per SM>
 template <int DQK, int DV, bool kNCHW, int QB, int ST, int CPS>
 cudaError_t run_dq(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                   const CUtensorMap& mDO, const BwdArgs& a, cudaStream_t st) {
+                   const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
+                   cudaStream_t st) {
   using Cfg = DqCfg<DQK, DV, kNCHW, QB, ST, CPS>;
-  return launch<Cfg, CPS>(attn_bwd_dq_kernel<DQK, DV, kNCHW, QB, ST, CPS>, mQ, mK, mV, mDO, a,
-                          Cfg::BM, st);
+  return launch<Cfg, CPS>(attn_bwd_dq_kernel<DQK, DV, kNCHW, QB, ST, CPS>, a, Cfg::BM, st, mQ,
+                          mK, mV, mDO, mO);
 }
 template <int DQK, int DV, bool kNCHW, int KB, int ST, int CPS>
 cudaError_t run_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                      const CUtensorMap& mDO, const BwdArgs& a, cudaStream_t st) {
   using Cfg = DkvCfg<DQK, DV, kNCHW, KB, ST, CPS>;
-  return launch<Cfg, CPS>(attn_bwd_dkdv_kernel<DQK, DV, kNCHW, KB, ST, CPS>, mQ, mK, mV, mDO, a,
-                          Cfg::BM, st);
+  return launch<Cfg, CPS>(attn_bwd_dkdv_kernel<DQK, DV, kNCHW, KB, ST, CPS>, a, Cfg::BM, st, mQ,
+                          mK, mV, mDO);
 }
 
 }  // namespace
@@ -740,8 +783,9 @@ cudaError_t launch_fa2_bwd_dq(const CUtensorMap& mQ, const CUtensorMap& mK,
                               const CUtensorMap& mV, const CUtensorMap& mDO, const BwdArgs& a,
                               int BH, int d, cudaStream_t st) {
   (void)BH;
-  if (d == 32) return run_dq<32, 32, false, 2, 4, 2>(mQ, mK, mV, mDO, a, st);
-  return run_dq<64, 64, false, 1, 2, 2>(mQ, mK, mV, mDO, a, st);
+  // raw planes: delta from vector global loads, no O tile (mDO stands in for it)
+  if (d == 32) return run_dq<32, 32, false, 2, 4, 2>(mQ, mK, mV, mDO, mDO, a, st);
+  return run_dq<64, 64, false, 1, 2, 2>(mQ, mK, mV, mDO, mDO, a, st);
 }
 
 cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
@@ -753,11 +797,11 @@ cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
 }
 
 cudaError_t launch_psa_bwd_dq(const CUtensorMap& mQK, const CUtensorMap& mV,
-                              const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
-                              cudaStream_t st) {
+                              const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
+                              int BH, int KD, cudaStream_t st) {
   (void)BH;
-  if (KD == 32) return run_dq<32, 64, true, 1, 4, 2>(mQK, mQK, mV, mDO, a, st);
-  return run_dq<64, 128, true, 2, 3, 1>(mQK, mQK, mV, mDO, a, st);
+  if (KD == 32) return run_dq<32, 64, true, 1, 3, 2>(mQK, mQK, mV, mDO, mO, a, st);
+  return run_dq<64, 128, true, 1, 3, 1>(mQK, mQK, mV, mDO, mO, a, st);
 }
 
 cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
