@@ -1,11 +1,14 @@
 """Benchmark of the PSA attention step (fused forward + dQ + dK/dV backward) on GB300.
 
-One step = psa_attention_fwd (QKV -> Out, LSE, extracted V) + psa_attention_bwd_dq
-+ psa_attention_bwd_dkdv (-> dQKV) over one batch of the 'psa_fwdbwd_n400'
-workload: B=64, num_heads=4, KEY_DIM=32, 20x20 (N=400), bf16, synthetic seeded
-N(0,1) inputs.  Prints ONE JSON line (rank 0).
+One step = psa_attention_fwd (QKV -> Out, LSE, extracted V) + psa_attention_bwd
+(-> dQKV; for this sequence length one kernel per head computes dQ, dK and dV)
+over one batch of the 'psa_fwdbwd_n400' workload: B=64, num_heads=4, KEY_DIM=32,
+20x20 (N=400), bf16, synthetic seeded N(0,1) inputs.  Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--split-bwd]
+
+--split-bwd times the two-kernel backward instead (psa_attention_bwd_dq then
+psa_attention_bwd_dkdv), the form that long sequences use.
 
 --impl reference times the fp64 CPU oracle (the test oracle, untuned) on the
 host cores, on a bounded sample of the same workload per step.
@@ -57,6 +60,9 @@ def work_model(w):
             (Q, K, V planes), Out, dOut, LSE; writes dQ and delta.
     bwd_dkdv: S^T, dP^T, dV = P^T dO (2 N^2 2KD), dK = dS^T Q (2 N^2 KD); reads QKV,
             dOut, LSE, delta; writes dK, dV.
+    bwd   : the one-kernel backward: S^T, dP^T, dV, dK and dQ = dS K once each per
+            head (2 N^2 (KD + 2KD + 2KD + KD + KD)); reads QKV, Out, dOut, LSE;
+            writes dQKV.
     step  : the algorithmic total (S computed once in the forward and once in the
             backward): 192 N^2 + 448 N^2 FLOPs per head; bytes = QKV + Out + V
             written, QKV + Out + dOut read and dQKV written, LSE written and read.
@@ -72,6 +78,7 @@ def work_model(w):
                    "bytes": B * N * (C + c + c + KD * w.num_heads) * e + 2 * lse},
         "bwd_dkdv": {"flops": n2 * (2 * KD + 2 * 2 * KD + 2 * 2 * KD + 2 * KD),
                      "bytes": B * N * (C + c + 3 * KD * w.num_heads) * e + 2 * lse},
+        "bwd": {"flops": n2 * 2 * 7 * KD, "bytes": B * N * (C + c + c + C) * e + lse},
     }
     step = {"flops": n2 * (192 / 32 * KD + 448 / 32 * KD),
             "bytes": B * N * (C + c + c) * e + lse + B * N * (C + c + c + C) * e + lse}
@@ -169,6 +176,8 @@ def run_ours(args, rank, world, local_rank):
             "lse": torch.empty((w.BH, w.N), dtype=torch.float32, device="cuda"),
             "delta": torch.empty((w.BH, w.N), dtype=torch.float32, device="cuda"),
             "dqkv": torch.empty_like(qkv),
+            "ws": torch.empty(B.psa_attention_bwd_workspace_size(shape), dtype=torch.uint8,
+                              device="cuda"),
         })
     stream = torch.cuda.current_stream()
 
@@ -183,8 +192,16 @@ def run_ours(args, rank, world, local_rank):
         B.psa_attention_bwd_dkdv(s["qkv"], s["dout"], s["lse"], s["delta"], None, s["dqkv"], shape, scale,
                                  stream)
 
-    parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
-    launches_per_step = 1 + 1 + 1  # forward (with PsaExtractV fused), dQ, dK/dV
+    def bwd(s):
+        B.psa_attention_bwd(s["qkv"], s["out"], s["dout"], s["lse"], None, s["dqkv"], s["ws"], shape,
+                            scale, stream)
+
+    if args.split_bwd:
+        parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
+    else:
+        parts = (("fwd", fwd), ("bwd", bwd))
+    # one launch each: the forward (PsaExtractV fused), and each backward kernel
+    launches_per_step = len(parts)
 
     def barrier():
         torch.cuda.synchronize()
@@ -200,7 +217,7 @@ def run_ours(args, rank, world, local_rank):
     if B.psa_get_last_device_error() != 0:
         raise RuntimeError("device error during warm-up")
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank)
     with sampler:
@@ -209,12 +226,9 @@ def run_ours(args, rank, world, local_rank):
             s = sets[i % nsets]
             e = ev[i]
             e[0].record(stream)
-            fwd(s)
-            e[1].record(stream)
-            bwd_dq(s)
-            e[2].record(stream)
-            bwd_dkdv(s)
-            e[3].record(stream)
+            for j, (_, f) in enumerate(parts):
+                f(s)
+                e[j + 1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
     ms_total = start.elapsed_time(stop)
@@ -242,9 +256,8 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(Ke):
         s["qkv"].copy_(h_qkv, non_blocking=True)
         s["dout"].copy_(h_dout, non_blocking=True)
-        fwd(s)
-        bwd_dq(s)
-        bwd_dkdv(s)
+        for _, f in parts:
+            f(s)
         h_out.copy_(s["out"], non_blocking=True)
         h_vres.copy_(s["vres"], non_blocking=True)
         h_lse.copy_(s["lse"], non_blocking=True)
@@ -288,7 +301,9 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) QKV and dOut)",
         "config": {"workload": WORKLOAD, "B": w.B, "num_heads": w.num_heads, "key_dim": w.key_dim,
                    "H": w.H, "W": w.W, "N": w.N, "global_batch": w.B * world, "seq_len": w.N,
-                   "parallelism": f"replicas x{world}", "l2": f"rotating {nsets} input/output sets "
+                   "parallelism": f"replicas x{world}",
+                   "backward": "two kernels (dQ, dK/dV)" if args.split_bwd else "psa_attention_bwd",
+                   "l2": f"rotating {nsets} input/output sets "
                    f"({nsets * per_set / 1e6:.0f} MB > 2 x L2)"},
         "tflops": tflops,
         "step_roofline": {"frac": step_roof_time / (ms_step / 1e3), "roofline_us": step_roof_time * 1e6,
@@ -388,6 +403,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--split-bwd", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -98,6 +98,8 @@ RAGGED = [
     # (B, nh, KD, H, W): N = 8, 40, 136, 144 (KD = 64), 264, 72
     (1, 1, 32, 2, 4), (2, 3, 32, 5, 8), (1, 2, 32, 8, 17), (2, 1, 64, 12, 12), (1, 2, 32, 12, 22),
     (3, 2, 64, 8, 9),
+    # KD = 32 around the one-kernel backward's tiles and its limit: N = 128, 512, 520
+    (2, 1, 32, 8, 16), (1, 2, 32, 16, 32), (1, 1, 32, 4, 130),
 ]
 
 
@@ -111,6 +113,37 @@ def test_psa_ragged_bf16(oracle, Bn, nh, KD, H, W):
 def test_psa_ragged_f32(oracle, Bn, nh, KD, H, W):
     ins = psa_inputs(Bn, nh, KD, H, W, "f32", seed=400 + H * W, with_grad=False)
     check_psa(oracle, ins, nh, KD, "f32", 1 / math.sqrt(KD), False)
+
+
+@pytest.mark.parametrize("Bn,nh,KD,H,W", [(2, 3, 32, 5, 8), (1, 2, 32, 20, 20), (2, 1, 64, 12, 12)])
+def test_split_backward_entry_points(oracle, Bn, nh, KD, H, W):
+    """psa_attention_bwd_dq then psa_attention_bwd_dkdv (the two-kernel backward that
+    psa_attention_bwd replaces by one kernel for short KD = 32 sequences)."""
+    import torch
+
+    scale = 1 / math.sqrt(KD)
+    ins = psa_inputs(Bn, nh, KD, H, W, "bf16", seed=500 + H * W, with_dvres=True)
+    qkv = to_device(ins["qkv"], "bf16")
+    out, lse, _ = fused_fwd(qkv, nh, KD, scale, with_v=False)
+    dout = to_device(ins["dout"], "bf16")
+    dvres = to_device(ins["dvres"], "bf16")
+    shape = B.shape_of(qkv, nh, KD)
+    delta = torch.empty((Bn * nh, H * W), dtype=torch.float32, device="cuda")
+    dqkv = torch.empty_like(qkv)
+    B.psa_attention_bwd_dq(qkv, out, dout, lse, delta, dqkv, shape, scale)
+    B.psa_attention_bwd_dkdv(qkv, dout, lse, delta, dvres, dqkv, shape, scale)
+    torch.cuda.synchronize()
+    q64 = storage_to_f64(ins["qkv"], "bf16")
+    ref = oracle.psa_bwd(q64, storage_to_f64(ins["dout"], "bf16"), nh, KD, scale,
+                         dvres=storage_to_f64(ins["dvres"], "bf16")).reshape(Bn, nh, 4, KD, -1)
+    got = to_host_f64(dqkv).reshape(Bn, nh, 4, KD, -1)
+    for s, name in enumerate(("dQ", "dK", "dV_lo", "dV_hi")):
+        assert_close(got[:, :, s], ref[:, :, s], "bf16", "split " + name, output_rounding=s >= 2)
+    fused = fused_bwd(qkv, out, dout, lse, dvres, nh, KD, scale)
+    torch.cuda.synchronize()
+    for s, name in enumerate(("dQ", "dK", "dV_lo", "dV_hi")):
+        assert_close(to_host_f64(fused).reshape(Bn, nh, 4, KD, -1)[:, :, s], ref[:, :, s], "bf16",
+                     "fused " + name, output_rounding=s >= 2)
 
 
 def test_unfused_chain_matches_oracle_and_fused(oracle):

@@ -78,4 +78,11 @@ cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st);
 
+// One-kernel backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxN):
+// same maps as launch_psa_bwd_dq; a.delta is not used.
+constexpr int kFusedBwdMaxN = 512;
+cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
+                                 const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
+                                 int KD, cudaStream_t st);
+
 }  // namespace psa

@@ -50,34 +50,6 @@ __device__ __forceinline__ int unit_count(int slot, int nslots, int T) {
   return slot < T ? (T - slot + nslots - 1) / nslots : 0;
 }
 
-// Loads a 64-column S row and the matching dP row (TMEM columns tS, tP) with
-// one wait; columns >= kend were not written and are not loaded.
-__device__ __forceinline__ void load_sp_rows(uint32_t tS, uint32_t tP, int kend,
-                                             uint32_t (&s)[64], uint32_t (&p)[64]) {
-  using Chunk = uint32_t[32];
-  tmem_load32_async(tS, *reinterpret_cast<Chunk*>(s));
-  tmem_load32_async(tP, *reinterpret_cast<Chunk*>(p));
-  if (kend > 32) {
-    tmem_load32_async(tS + 32, *reinterpret_cast<Chunk*>(s + 32));
-    tmem_load32_async(tP + 32, *reinterpret_cast<Chunk*>(p + 32));
-  }
-  tmem_wait_ld();
-  tmem_pin(*reinterpret_cast<Chunk*>(s));
-  tmem_pin(*reinterpret_cast<Chunk*>(p));
-  tmem_pin(*reinterpret_cast<Chunk*>(s + 32));
-  tmem_pin(*reinterpret_cast<Chunk*>(p + 32));
-}
-
-// Stores 8 packed bf16x2 words per 16-byte chunk of a 128-row, 64-column K-major
-// tile with the 128-byte swizzle (row r, chunks below kend / 8).
-__device__ __forceinline__ void store_row64(uint32_t tile, int r, int kend, const uint32_t* w) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch)
-    if (ch * 8 < kend)
-      st_shared_v4(tile + swizzled_offset(r, ch, 128), w[ch * 4], w[ch * 4 + 1], w[ch * 4 + 2],
-                   w[ch * 4 + 3]);
-}
-
 // ====================================================================== dQ
 template <int DQK, int DV, bool kNCHW, int QBUF, int ST, int CPS>
 struct DqCfg {
