@@ -200,8 +200,10 @@ def run_ours(args, rank, world, local_rank):
         parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
     else:
         parts = (("fwd", fwd), ("bwd", bwd))
-    # one launch each: the forward (PsaExtractV fused), and each backward kernel
-    launches_per_step = len(parts)
+    # kernels per call: the forward (PsaExtractV fused) 1; psa_attention_bwd at this
+    # sequence length 2 (delta pass + one-kernel backward); dQ 1; dK/dV 1
+    launches = {"fwd": 1, "bwd": 2, "bwd_dq": 1, "bwd_dkdv": 1}
+    launches_per_step = sum(launches[name] for name, _ in parts)
 
     def barrier():
         torch.cuda.synchronize()

@@ -396,10 +396,10 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
   if (e != PSA_OK) return e;
   const int BH = s.B * s.num_heads;
   if (s.key_dim == 32 && s.H * s.W <= psa::kFusedBwdMaxN) {
-    // short sequences: one kernel per head produces dQ, dK and dV from a single
-    // pass (delta stays on chip; the workspace is not touched)
+    // short sequences: after a delta pass, one kernel per head produces dQ, dK
+    // and dV from a single walk over its tiles
     a_dq.dvres = static_cast<const __nv_bfloat16*>(dvres);
-    return from_cuda(psa::launch_psa_bwd_fused(mqk, mv, mdo, mo, a_dq, s.key_dim, st));
+    return from_cuda(psa::launch_psa_bwd_fused(mqk, mv, mdo, a_dq, s.key_dim, st));
   }
   e = from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, mo, a_dq, BH, s.key_dim, st));
   if (e != PSA_OK) return e;

@@ -78,11 +78,12 @@ cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st);
 
-// One-kernel backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxN):
-// same maps as launch_psa_bwd_dq; a.delta is not used.
+// Backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxN, N % 8 == 0):
+// a delta pass over Out / dOut into a.delta, then one kernel for dQ, dK and dV.
+// Same maps as launch_psa_bwd_dkdv.
 constexpr int kFusedBwdMaxN = 512;
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
-                                 const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
-                                 int KD, cudaStream_t st);
+                                 const CUtensorMap& mDO, const BwdArgs& a, int KD,
+                                 cudaStream_t st);
 
 }  // namespace psa

@@ -7,26 +7,29 @@
 //   P = exp(scale q k^T - lse),  dP = dO V^T,  dS = P o (dP - delta),
 //   delta_i = sum_c dO_ic O_ic,  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
 // but from a single pass over the (key tile, query tile) pairs of a head: each
-// P / dS tile is produced once and feeds all three gradients.  Split into two
-// kernels, every P and dP is computed twice (once per kernel); here they are
-// not, and delta never leaves the chip.  dQ of every query tile of the head stays
-// in tensor memory for the whole walk (4 x 32 columns), which is what bounds N.
+// P / dS tile is produced once and feeds all three gradients.  (Split into two
+// kernels, every P and dP is computed twice.)  dQ of every query tile of the
+// head stays in tensor memory for the whole walk (4 x 32 columns), which is
+// what bounds N.
+//
+// Two launches: psa_bwd_delta_kernel writes delta = rowsum(dO o O) (a
+// bandwidth-bound pass over Out and dOut), then the fused kernel.
 //
 // Layout: QKV / Out / dOut in NCHW, dQKV written in NCHW (the adjoints of
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing, the optional
 // PsaExtractV gradient is added into the V channels), as in the split kernels.
 //
-// One CTA per SM (persistent over heads), 320 threads:
+// Fused kernel: one CTA per SM (persistent over heads), 352 threads:
 //   warps 0-7  row threads: warp w serves TMEM lanes 32(w%4).. (key rows) and
 //              query columns 64(w/4)..+63 of the 128 x 128 S^T / dP^T tiles;
-//              they build P^T and dS^T (bf16) in shared memory, compute delta
-//              of each query tile on the first key tile, and write dK, dV per
-//              key tile and dQ per head;
+//              they build P^T and dS^T (bf16) in shared memory and write dK, dV
+//              per key tile and dQ per head;
 //   warp 8     TMA producer (K / V per key tile, double-buffered; Q / dO per
-//              step in a ring; O and lse per query tile on the first key tile);
-//   warp 9     issues every tcgen05.mma and owns the 512 TMEM columns:
-//              S^T = K Q^T (128 cols), dP^T = V dO^T (128), dV (64), dK (32),
-//              dQ of up to 4 query tiles (4 x 32).
+//              step in a ring, with the step's lse and delta loaded by all lanes);
+//   warp 9     issues S^T = K Q^T (128 TMEM cols) and dP^T = V dO^T (128) and
+//              owns the 512 TMEM columns;
+//   warp 10    issues the gradient products into dV (64), dK (32) and dQ of up
+//              to 4 query tiles (4 x 32).
 // Per step (key tile kt, query tile qt):  S^T, dP^T  ->  row threads  ->
 //   dV += P^T dO,  dK += dS^T Q,  dQ_qt += dS K  (dS read as the MN-major
 //   view of the dS^T tile).  The next step's S^T / dP^T is issued as soon as
@@ -47,6 +50,39 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
 
+// ---------------------------------------------------------------------- delta
+// delta[bh, q] = sum_c Out[b, head c, q] * dOut[b, head c, q] over the 2*KD output
+// channels of head bh (NCHW, positions contiguous): eight positions per thread.
+template <int DV>
+__global__ void __launch_bounds__(128) psa_bwd_delta_kernel(const BwdArgs args) {
+  const int N = args.N;
+  const int groups = N / 8;  // N is a multiple of 8
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (long long)args.BH * groups) return;
+  const int bh = (int)(t / groups), q0 = (int)(t % groups) * 8;
+  const long long row = (long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV;
+  const __nv_bfloat16* o = args.o + row * N + q0;
+  const __nv_bfloat16* g = args.dO + row * N + q0;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int c = 0; c < DV; ++c) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + (long long)c * N);
+    const uint4 gv = *reinterpret_cast<const uint4*>(g + (long long)c * N);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+      acc[2 * e] = fmaf(of.x, gf.x, acc[2 * e]);
+      acc[2 * e + 1] = fmaf(of.y, gf.y, acc[2 * e + 1]);
+    }
+  }
+  float4* d = reinterpret_cast<float4*>(args.delta + (long long)bh * N + q0);
+  d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// ---------------------------------------------------------------------- fused
 // One 32-column chunk of this lane's S^T and dP^T rows, loaded with one wait.
 __device__ __forceinline__ void load_sp_chunk(uint32_t tS, uint32_t tP, uint32_t (&sv)[32],
                                               uint32_t (&pv)[32]) {
@@ -83,19 +119,18 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[32], const uint3
 template <int DQK, int DV, int ST>
 struct FusedCfg {
   static constexpr int BK = 128, BQ = 128, MAXN = kFusedBwdMaxN, MAXT = MAXN / BQ;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr uint32_t K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
-  static constexpr uint32_t Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2, O_BYTES = BQ * DV * 2;
+  static constexpr uint32_t Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
   static constexpr uint32_t STAGE_BYTES = Q_BYTES + DO_BYTES;
   static constexpr uint32_t HALF_BYTES = BK * 64 * 2;  // 64 query columns of P^T or dS^T
   static constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + 2 * K_BYTES;
   static constexpr uint32_t OFF_STAGE = OFF_V + 2 * V_BYTES;
-  static constexpr uint32_t OFF_O = OFF_STAGE + ST * STAGE_BYTES;
-  static constexpr uint32_t OFF_PT = OFF_O + O_BYTES;
+  static constexpr uint32_t STAT_BYTES = 2 * BQ * 4;  // lse2[128], delta[128] of a stage
+  static constexpr uint32_t OFF_PT = OFF_STAGE + ST * STAGE_BYTES;
   static constexpr uint32_t OFF_DST = OFF_PT + 2 * HALF_BYTES;
-  static constexpr uint32_t OFF_OLSE = OFF_DST + 2 * HALF_BYTES;  // lse2 of the O tile's queries
-  static constexpr uint32_t OFF_HST = OFF_OLSE + BQ * 4;  // [head parity][lse2 | delta][MAXN]
-  static constexpr uint32_t OFF_BAR = OFF_HST + 2 * 2 * MAXN * 4;
+  static constexpr uint32_t OFF_STAT = OFF_DST + 2 * HALF_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_STAT + ST * STAT_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = TM_DV + DV;
   static constexpr uint32_t TM_DQ = TM_DK + DQK;
@@ -106,8 +141,7 @@ struct FusedCfg {
 
 struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[4], q_empty[4];
-  uint64_t o_full, o_empty, st_ready[2];
-  uint64_t s_full, s_free, p_full, pds_free, acc_full, acc_free, mma_done;
+  uint64_t s_full, s_free, p_full, pds_free, acc_full, acc_free, mma_done[2];
 };
 
 // Descriptor address steps (16-byte units) of the k-th 16-element K step.
@@ -124,12 +158,11 @@ __device__ __forceinline__ uint64_t off_ch_by_pos(int kk) {
 }
 
 template <int DQK, int DV, int ST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
-                          const __grid_constant__ CUtensorMap tmDO,
-                          const __grid_constant__ CUtensorMap tmO, const BwdArgs args) {
+                          const __grid_constant__ CUtensorMap tmDO, const BwdArgs args) {
   using C = FusedCfg<DQK, DV, ST>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -152,21 +185,19 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.kv_full[i], 1);
       mbar_init(&b.kv_empty[i], 1);
-      mbar_init(&b.st_ready[i], 128);
     }
     for (int i = 0; i < ST; ++i) {
-      mbar_init(&b.q_full[i], 1);
+      mbar_init(&b.q_full[i], 1 + 32);
       mbar_init(&b.q_empty[i], 1);
     }
-    mbar_init(&b.o_full, 1 + 32);
-    mbar_init(&b.o_empty, 128);
     mbar_init(&b.s_full, 1);
     mbar_init(&b.s_free, 256);
     mbar_init(&b.p_full, 256);
     mbar_init(&b.pds_free, 1);
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.acc_free, 256);
-    mbar_init(&b.mma_done, 1);
+    mbar_init(&b.mma_done[0], 1);
+    mbar_init(&b.mma_done[1], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -181,20 +212,22 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // K / V by lane 0; the lse of an O tile by all lanes (33 arrivals complete
-    // o_full), fetched one O tile ahead into registers.
+    // K / V and Q / dO by lane 0; lse2 / delta of the step's 128 queries by all
+    // lanes (33 arrivals complete a stage), fetched one stage ahead.
     bool ok = true;
-    int kvc = 0, qc = 0, oc = 0;
-    float pl[4];
-    auto prefetch_lse = [&](int u, int qt) {
+    int kvc = 0, qc = 0;
+    float pl[4], pd[4];
+    auto prefetch_stats = [&](int u, int qt) {
       const int bh = head_of(u);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int q = qt * C::BQ + lane + 32 * h;
-        pl[h] = q < N ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
+        const bool in = q < N;
+        pl[h] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
+        pd[h] = in ? args.delta[(long long)bh * N + q] : 0.f;
       }
     };
-    if (nunits > 0) prefetch_lse(0, 0);
+    if (nunits > 0) prefetch_stats(0, 0);
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
       for (int kt = 0; ok && kt < nt; ++kt) {
@@ -224,37 +257,33 @@ __global__ void __launch_bounds__(320, 1)
             load_tile<true, DV>(stage + C::Q_BYTES, &tmDO, &b.q_full[st], C::BQ, qt * C::BQ, bh,
                                 out_row(bh));
           }
-          ++qc;
-          if (kt == 0) {
-            if (oc >= 1 && !mbar_wait(&b.o_empty, (oc - 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            float* olse = reinterpret_cast<float*>(smem + C::OFF_OLSE);
+          float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) olse[lane + 32 * h] = pl[h];
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&b.o_full, C::O_BYTES);
-              load_tile<true, DV>(smem + C::OFF_O, &tmO, &b.o_full, C::BQ, qt * C::BQ, bh,
-                                  out_row(bh));
-            }
-            mbar_arrive(&b.o_full);
-            ++oc;
-            if (qt + 1 < nt)
-              prefetch_lse(u, qt + 1);
-            else if (u + 1 < nunits)
-              prefetch_lse(u + 1, 0);
+          for (int h = 0; h < 4; ++h) {
+            stat[lane + 32 * h] = pl[h];
+            stat[C::BQ + lane + 32 * h] = pd[h];
           }
+          mbar_arrive(&b.q_full[st]);
+          ++qc;
+          if (qt + 1 < nt)
+            prefetch_stats(u, qt + 1);
+          else if (kt + 1 < nt)
+            prefetch_stats(u, 0);
+          else if (u + 1 < nunits)
+            prefetch_stats(u + 1, 0);
         }
       }
     }
     if (lane == 0 && *abort) {
       for (int i = max(0, kvc - 2); i < kvc; ++i) drain_wait(&b.kv_full[i & 1], (i >> 1) & 1);
       for (int i = max(0, qc - ST); i < qc; ++i) drain_wait(&b.q_full[i % ST], (i / ST) & 1);
-      if (oc > 0) drain_wait(&b.o_full, (oc - 1) & 1);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads share the tensor pipe: warp 9 issues S^T / dP^T, warp
+    // 10 the gradient products, so the waits of one stream are covered by the
+    // other's MMAs (a thread that waits issues nothing, and the pipe holds
+    // little more than the MMA it is executing).
     if (lane == 0) {
       const uint64_t dK0 = desc_mnmajor(tile_view<true, DQK>(sbase + C::OFF_K, C::BK), 0);
       const uint64_t dV0 = desc_mnmajor(tile_view<true, DV>(sbase + C::OFF_V, C::BK), 0);
@@ -332,24 +361,14 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
 
-      bool ok = nunits > 0 ? issue_sdp(0, 0, 0) : true;
+      // steps in order: qt fastest, then kt, then head
+      bool ok = true;
       for (int u = 0; ok && u < nunits; ++u)
         for (int kt = 0; ok && kt < nt; ++kt)
-          for (int qt = 0; ok && qt < nt; ++qt) {
-            // successor step (qt fastest, then kt, then head)
-            int u1 = u, kt1 = kt, qt1 = qt + 1;
-            if (qt1 == nt) {
-              qt1 = 0;
-              if (++kt1 == nt) {
-                kt1 = 0;
-                ++u1;
-              }
-            }
-            if (u1 < nunits) ok = issue_sdp(u1, kt1, qt1);
-            if (ok) ok = issue_grad(u, kt, qt);
-          }
-      mma_commit(&b.mma_done);
-      drain_wait(&b.mma_done, 0);
+          for (int qt = 0; ok && qt < nt; ++qt)
+            ok = warp == 9 ? issue_sdp(u, kt, qt) : issue_grad(u, kt, qt);
+      mma_commit(&b.mma_done[warp - 9]);
+      drain_wait(&b.mma_done[warp - 9], 0);
     }
   } else {
     // ------------------------------------------------------------ row threads
@@ -359,11 +378,8 @@ __global__ void __launch_bounds__(320, 1)
     const int c0 = half * 64;      // first query column of this thread
     const float sl2 = args.scale_log2, sc = args.scale;
     bool ok = true;
-    int oc = 0;
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
-      float* lse2_h = reinterpret_cast<float*>(smem + C::OFF_HST) + (u & 1) * 2 * C::MAXN;
-      float* dl_h = lse2_h + C::MAXN;
       for (int kt = 0; ok && kt < nt; ++kt) {
         const int kvi = u * nt + kt;
         const int vk = min(C::BK, N - kt * C::BK);
@@ -374,40 +390,8 @@ __global__ void __launch_bounds__(320, 1)
           const int mine = vq - c0;
           const int kend = mine > 0 ? (min(mine, 64) + 15) & ~15 : 0;
           const bool active = krows && mine > 0;
-          if (kt == 0) {
-            // delta and lse2 of query tile qt (one query per thread of warps 0-3)
-            if (half == 0) {
-              if (!mbar_wait(&b.o_full, oc & 1, abort) ||
-                  !mbar_wait(&b.q_full[st], (s / ST) & 1, abort)) {
-                ok = false;
-                break;
-              }
-              const int q = qt * C::BQ + r;
-              float D = 0.f;
-              if (q < N) {
-                const unsigned char* to = smem + C::OFF_O + (r >> 6) * (DV * 128);
-                const unsigned char* tg =
-                    smem + C::OFF_STAGE + st * C::STAGE_BYTES + C::Q_BYTES + (r >> 6) * (DV * 128);
-                const int p = r & 63;
-#pragma unroll 16
-                for (int c = 0; c < DV; ++c) {
-                  const uint32_t off = swizzled_offset(c, p >> 3, 128) + (p & 7) * 2;
-                  D = fmaf(bf(*reinterpret_cast<const __nv_bfloat16*>(to + off)),
-                           bf(*reinterpret_cast<const __nv_bfloat16*>(tg + off)), D);
-                }
-              }
-              lse2_h[q] = reinterpret_cast<const float*>(smem + C::OFF_OLSE)[r];
-              dl_h[q] = D;
-              mbar_arrive(&b.o_empty);
-              mbar_arrive(&b.st_ready[oc & 1]);
-            }
-            if (!mbar_wait(&b.st_ready[oc & 1], (oc >> 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            ++oc;
-          }
-          if (!mbar_wait(&b.s_full, s & 1, abort)) {
+          if (!mbar_wait(&b.s_full, s & 1, abort) ||
+              !mbar_wait(&b.q_full[st], (s / ST) & 1, abort)) {
             ok = false;
             break;
           }
@@ -416,8 +400,9 @@ __global__ void __launch_bounds__(320, 1)
           // which keeps at most 96 row values live.  S^T / dP^T go back to the MMA
           // warp once both chunks are in registers.
           uint32_t pw[32], dw[32];  // packed P^T and dS^T of the 64 columns
-          const float* lrow = lse2_h + qt * C::BQ + c0;
-          const float* drow = dl_h + qt * C::BQ + c0;
+          const float* lrow =
+              reinterpret_cast<const float*>(smem + C::OFF_STAT + st * C::STAT_BYTES) + c0;
+          const float* drow = lrow + C::BQ;
           const uint32_t tS = tmem + lane_base + C::TM_ST + c0;
           const uint32_t tP = tmem + lane_base + C::TM_DPT + c0;
           if (active) {
@@ -523,16 +508,21 @@ __global__ void __launch_bounds__(320, 1)
 }  // namespace
 
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
-                                 const CUtensorMap& mDO, const CUtensorMap& mO, const BwdArgs& a,
-                                 int KD, cudaStream_t st) {
-  if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.BH <= 0) return cudaErrorInvalidValue;
-  using Cfg = FusedCfg<32, 64, 3>;
-  auto kern = attn_bwd_fused_kernel<32, 64, 3>;
+                                 const CUtensorMap& mDO, const BwdArgs& a, int KD,
+                                 cudaStream_t st) {
+  if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.delta)
+    return cudaErrorInvalidValue;
+  const long long threads = (long long)a.BH * (a.N / 8);
+  psa_bwd_delta_kernel<64><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  using Cfg = FusedCfg<32, 64, 4>;
+  auto kern = attn_bwd_fused_kernel<32, 64, 4>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   const int ctas = std::min(device_sm_count(), a.BH);
-  kern<<<ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQK, mQK, mV, mDO, mO, a);
+  kern<<<ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQK, mQK, mV, mDO, a);
   return cudaGetLastError();
 }
 
