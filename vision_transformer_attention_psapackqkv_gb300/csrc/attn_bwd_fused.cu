@@ -22,8 +22,8 @@
 // Fused kernel: one CTA per SM (persistent over heads), 352 threads:
 //   warps 0-7  row threads: warp w serves TMEM lanes 32(w%4).. (key rows) and
 //              query columns 64(w/4)..+63 of the 128 x 128 S^T / dP^T tiles;
-//              they build P^T and dS^T (bf16) in shared memory and write dK, dV
-//              per key tile and dQ per head;
+//              they build P^T and dS^T (bf16, dS^T double-buffered) in shared
+//              memory and write dK, dV per key tile and dQ per head;
 //   warp 8     TMA producer (K / V per key tile, double-buffered; Q / dO per
 //              step in a ring, with the step's lse and delta loaded by all lanes);
 //   warp 9     issues S^T = K Q^T (128 TMEM cols) and dP^T = V dO^T (128) and
@@ -128,8 +128,9 @@ struct FusedCfg {
   static constexpr uint32_t OFF_STAGE = OFF_V + 2 * V_BYTES;
   static constexpr uint32_t STAT_BYTES = 2 * BQ * 4;  // lse2[128], delta[128] of a stage
   static constexpr uint32_t OFF_PT = OFF_STAGE + ST * STAGE_BYTES;
-  static constexpr uint32_t OFF_DST = OFF_PT + 2 * HALF_BYTES;
-  static constexpr uint32_t OFF_STAT = OFF_DST + 2 * HALF_BYTES;
+  static constexpr uint32_t PAIR_BYTES = 2 * HALF_BYTES;  // one buffer of P^T or dS^T
+  static constexpr uint32_t OFF_DST = OFF_PT + PAIR_BYTES;  // dS^T: two buffers (step parity)
+  static constexpr uint32_t OFF_STAT = OFF_DST + 2 * PAIR_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_STAT + ST * STAT_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = TM_DV + DV;
@@ -141,7 +142,7 @@ struct FusedCfg {
 
 struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[4], q_empty[4];
-  uint64_t s_full, s_free, p_full, pds_free, acc_full, acc_free, mma_done[2];
+  uint64_t s_full, s_free, p_full, pt_free, dst_free[2], acc_full, acc_free, mma_done[2];
 };
 
 // Descriptor address steps (16-byte units) of the k-th 16-element K step.
@@ -193,7 +194,9 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&b.s_full, 1);
     mbar_init(&b.s_free, 256);
     mbar_init(&b.p_full, 256);
-    mbar_init(&b.pds_free, 1);
+    mbar_init(&b.pt_free, 1);
+    mbar_init(&b.dst_free[0], 1);
+    mbar_init(&b.dst_free[1], 1);
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.acc_free, 256);
     mbar_init(&b.mma_done[0], 1);
@@ -213,23 +216,32 @@ __global__ void __launch_bounds__(352, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     // K / V and Q / dO by lane 0; lse2 / delta of the step's 128 queries by all
-    // lanes (33 arrivals complete a stage), fetched one stage ahead.
+    // lanes (33 arrivals complete a stage).  The lse / delta of a whole head sit
+    // in the lanes' registers (query lane + 32 i), loaded one head ahead, so no
+    // global-memory latency lands between two stages.
     bool ok = true;
     int kvc = 0, qc = 0;
-    float pl[4], pd[4];
-    auto prefetch_stats = [&](int u, int qt) {
+    constexpr int kPer = C::MAXN / 32;
+    float hl[kPer], hd[kPer], nl[kPer], nd[kPer];
+    auto load_head = [&](int u) {
       const int bh = head_of(u);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int q = qt * C::BQ + lane + 32 * h;
+      for (int i = 0; i < kPer; ++i) {
+        const int q = lane + 32 * i;
         const bool in = q < N;
-        pl[h] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
-        pd[h] = in ? args.delta[(long long)bh * N + q] : 0.f;
+        nl[i] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
+        nd[i] = in ? args.delta[(long long)bh * N + q] : 0.f;
       }
     };
-    if (nunits > 0) prefetch_stats(0, 0);
+    if (nunits > 0) load_head(0);
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        hl[i] = nl[i];
+        hd[i] = nd[i];
+      }
+      if (u + 1 < nunits) load_head(u + 1);
       for (int kt = 0; ok && kt < nt; ++kt) {
         const int kb = kvc & 1;
         if (kvc >= 2 && !mbar_wait(&b.kv_empty[kb], ((kvc >> 1) - 1) & 1, abort)) {
@@ -259,18 +271,14 @@ __global__ void __launch_bounds__(352, 1)
           }
           float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT + st * C::STAT_BYTES);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            stat[lane + 32 * h] = pl[h];
-            stat[C::BQ + lane + 32 * h] = pd[h];
+          for (int i = 0; i < kPer; ++i) {
+            if (i / 4 == qt) {
+              stat[lane + 32 * (i % 4)] = hl[i];
+              stat[C::BQ + lane + 32 * (i % 4)] = hd[i];
+            }
           }
           mbar_arrive(&b.q_full[st]);
           ++qc;
-          if (qt + 1 < nt)
-            prefetch_stats(u, qt + 1);
-          else if (kt + 1 < nt)
-            prefetch_stats(u, 0);
-          else if (u + 1 < nunits)
-            prefetch_stats(u + 1, 0);
         }
       }
     }
@@ -336,23 +344,27 @@ __global__ void __launch_bounds__(352, 1)
         const uint64_t dDOb = dDOb0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
         const uint64_t dKb = dKb0 + (uint64_t)(kb * C::K_BYTES >> 4);
         const int vq = min(C::BQ, N - qt * C::BQ), vk = min(C::BK, N - kt * C::BK);
+        // dV first, so P^T is released early; dS^T is double-buffered by step parity
+        const uint64_t dDST = dDST0 + (uint64_t)((s & 1) * C::PAIR_BYTES >> 4);
+        const uint64_t dDS = dDS0 + (uint64_t)((s & 1) * C::PAIR_BYTES >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          if (kk * 16 < vq) {
-            const uint32_t acc = (qt > 0 || kk > 0) ? 1u : 0u;
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          if (kk * 16 < vq)
             mma_bf16(tmem + C::TM_DV, dPT0 + off_kmajor_pair(kk), dDOb + off_ch_by_pos<DV>(kk),
-                     idDV, acc);
-            mma_bf16(tmem + C::TM_DK, dDST0 + off_kmajor_pair(kk), dQb + off_ch_by_pos<DQK>(kk),
-                     idDK, acc);
-          }
-        }
+                     idDV, (qt > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&b.pt_free);
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          if (kk * 16 < vq)
+            mma_bf16(tmem + C::TM_DK, dDST + off_kmajor_pair(kk), dQb + off_ch_by_pos<DQK>(kk),
+                     idDK, (qt > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           if (kk * 16 < vk)
-            mma_bf16(tmem + C::TM_DQ + qt * DQK, dDS0 + kk * kStepCh, dKb + off_ch_by_pos<DQK>(kk),
+            mma_bf16(tmem + C::TM_DQ + qt * DQK, dDS + kk * kStepCh, dKb + off_ch_by_pos<DQK>(kk),
                      idDQ, (kt > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&b.pds_free);
+        mma_commit(&b.dst_free[s & 1]);
         mma_commit(&b.q_empty[st]);
         if (qt == nt - 1) {
           mma_commit(&b.kv_empty[kb]);
@@ -423,14 +435,20 @@ __global__ void __launch_bounds__(352, 1)
             tc_fence_before();
             mbar_arrive(&b.s_free);
           }
-          if (s >= 1 && !mbar_wait(&b.pds_free, (s - 1) & 1, abort)) {
+          // P^T once the dV products of the previous step are done, dS^T once the
+          // dK / dQ products of two steps back are done
+          if (s >= 1 && !mbar_wait(&b.pt_free, (s - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          if (active) {
-            store_row64(sbase + C::OFF_PT + half * C::HALF_BYTES, r, kend, pw);
-            store_row64(sbase + C::OFF_DST + half * C::HALF_BYTES, r, kend, dw);
+          if (active) store_row64(sbase + C::OFF_PT + half * C::HALF_BYTES, r, kend, pw);
+          if (s >= 2 && !mbar_wait(&b.dst_free[s & 1], ((s >> 1) - 1) & 1, abort)) {
+            ok = false;
+            break;
           }
+          if (active)
+            store_row64(sbase + C::OFF_DST + (s & 1) * C::PAIR_BYTES + half * C::HALF_BYTES, r,
+                        kend, dw);
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&b.p_full);
@@ -516,8 +534,8 @@ cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
   psa_bwd_delta_kernel<64><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  using Cfg = FusedCfg<32, 64, 4>;
-  auto kern = attn_bwd_fused_kernel<32, 64, 4>;
+  using Cfg = FusedCfg<32, 64, 3>;
+  auto kern = attn_bwd_fused_kernel<32, 64, 3>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
