@@ -264,6 +264,17 @@ __device__ __forceinline__ void tmem_load32_async(uint32_t taddr, uint32_t (&r)[
       : "r"(taddr)
       : "memory");
 }
+// The same for 16 columns (32x32b.x16).
+__device__ __forceinline__ void tmem_load16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -278,7 +289,13 @@ __device__ __forceinline__ void tmem_pin(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
-// Stores 32 consecutive fp32 TMEM columns of this thread's lane and waits.
+__device__ __forceinline__ void tmem_pin(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
 // Stores 16 consecutive 32-bit TMEM columns of this thread's lane without waiting;
 // tmem_wait_st() makes the stores complete.
 __device__ __forceinline__ void tmem_store16_async(uint32_t taddr, const uint32_t* v) {
@@ -293,6 +310,7 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Stores 32 consecutive fp32 TMEM columns of this thread's lane and waits.
 __device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
