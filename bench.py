@@ -35,6 +35,11 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "psa_fwdbwd_n400"
 METRIC = "PSA attention fwd+bwd tokens/s and TFLOP/s at N=400, KEY_DIM=32; % roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per call of each step part, measured with ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum) on this workload for the current
+# kernels; to be re-measured whenever a kernel changes.
+MEASURED_TRAFFIC = {"fwd": 26.27e6, "bwd": 26.23e6 + 40.19e6 + 0.91e6,
+                    "bwd_dq": 52.88e6 + 0.33e6, "bwd_dkdv": 40.20e6 + 0.46e6}
 
 
 def load_peaks():
@@ -292,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": km["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = MEASURED_TRAFFIC.get(dom)
     roof["kernel"] = dom
     roof["peak_source"] = peak_src
     step_roof_time = max(step_model["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),

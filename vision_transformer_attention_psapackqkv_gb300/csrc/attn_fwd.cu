@@ -1,6 +1,6 @@
 // attn_fwd.cu -- Flash Attention 2 forward (vision-rs book, page "Custom Kernels",
 // section "Flash Attention 2"): O = softmax(scale * Q K^T) V with an online
-// softmax over key tiles; the N x N score matrix only ever exists one 128 x 128
+// softmax over key tiles; the N x N score matrix only ever exists one 128 x 64
 // tile at a time, in tensor memory.
 //
 // bf16 path (tcgen05, sm_103a): a persistent kernel.  Each CTA runs NWG
@@ -8,13 +8,16 @@
 // tiles t = s, s + S, s + 2S, ... (S = slots in the grid; tile t = head t / nqt,
 // query tile t % nqt).  Warp roles:
 //   warps 4w .. 4w+3   softmax of slot w: one thread per query row (= TMEM lane)
-//   warp 4*NWG         TMA producer: per slot, Q (double-buffered) and a 2-stage
-//                      K/V ring
+//   warp 4*NWG         TMA producer: per slot, Q (double- or single-buffered)
+//                      and a 2- to 4-stage ring of 64-key K/V tiles
 //   warp 4*NWG + 1     MMA issuer (one thread) and TMEM owner; per slot
-//                        S_k = Q K_k^T -> TMEM (128 columns)
-//                        O  += P_k V_k -> TMEM (DV columns), P_k from shared memory
-//                      S_{k+1} is issued as soon as the softmax has read S_k, so
-//                      it overlaps the exponentials of tile k.
+//                        S_k = Q K_k^T -> TMEM (64 columns)
+//                        O  += P_k V_k -> TMEM (DV columns), P_k from shared
+//                        memory (double-buffered)
+//                      S_{k+1} is issued as soon as the softmax holds S_k in
+//                      registers, so it overlaps the exponentials of tile k.
+// The bf16 kernels run persistent grids; with one slot per CTA two CTAs share
+// an SM (and its tensor core), which interleaves their softmax and MMA phases.
 // Softmax: running max in the log2 domain; p = 2^(scale*log2e*s - m) rounded to
 // bf16 into P (K-major, 128-byte swizzle); O is rescaled in TMEM only when a row
 // max grows by more than 2^8 (exact either way, since O and the running sum
