@@ -186,20 +186,20 @@ def run_ours(args, rank, world, local_rank):
         })
     stream = torch.cuda.current_stream()
 
-    def fwd(s):
-        B.psa_attention_fwd(s["qkv"], s["out"], s["lse"], s["vres"], shape, scale, stream)
+    def fwd(s, st=stream):
+        B.psa_attention_fwd(s["qkv"], s["out"], s["lse"], s["vres"], shape, scale, st)
 
-    def bwd_dq(s):
+    def bwd_dq(s, st=stream):
         B.psa_attention_bwd_dq(s["qkv"], s["out"], s["dout"], s["lse"], s["delta"], s["dqkv"], shape,
-                               scale, stream)
+                               scale, st)
 
-    def bwd_dkdv(s):
+    def bwd_dkdv(s, st=stream):
         B.psa_attention_bwd_dkdv(s["qkv"], s["dout"], s["lse"], s["delta"], None, s["dqkv"], shape, scale,
-                                 stream)
+                                 st)
 
-    def bwd(s):
+    def bwd(s, st=stream):
         B.psa_attention_bwd(s["qkv"], s["out"], s["dout"], s["lse"], None, s["dqkv"], s["ws"], shape,
-                            scale, stream)
+                            scale, st)
 
     if args.split_bwd:
         parts = (("fwd", fwd), ("bwd_dq", bwd_dq), ("bwd_dkdv", bwd_dkdv))
@@ -256,21 +256,86 @@ def run_ours(args, rank, world, local_rank):
     h_lse = torch.empty(sets[0]["lse"].shape, dtype=torch.float32).pin_memory()
     h_dqkv = torch.empty(sets[0]["dqkv"].shape, dtype=torch.bfloat16).pin_memory()
     Ke = max(3, min(K, 200))
-    s = sets[0]
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        s["qkv"].copy_(h_qkv, non_blocking=True)
-        s["dout"].copy_(h_dout, non_blocking=True)
-        for _, f in parts:
-            f(s)
+    # Steps are pipelined the way a caller streaming batches would: the inputs of
+    # step i+1 go up (copy stream `cin`) and the results of step i-1 come down
+    # (`cout`) while step i computes on `cs`; two device sets alternate, and
+    # events keep every copy and every call in order on its buffer.  The whole
+    # sequence of Ke steps is captured once into a CUDA graph and replayed, so
+    # host-side launch overhead stays out of the measurement.
+    # Each direction is split over two streams (two copy engines at once).
+    cs = torch.cuda.Stream()
+    cins = (torch.cuda.Stream(), torch.cuda.Stream())
+    couts = (torch.cuda.Stream(), torch.cuda.Stream())
+    bufs = (sets[0], sets[1 % nsets])
+    ev_in = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]
+    up = (lambda s: s["qkv"].copy_(h_qkv, non_blocking=True),
+          lambda s: s["dout"].copy_(h_dout, non_blocking=True))
+
+    def down0(s):
+        h_dqkv.copy_(s["dqkv"], non_blocking=True)
+
+    def down1(s):
         h_out.copy_(s["out"], non_blocking=True)
         h_vres.copy_(s["vres"], non_blocking=True)
         h_lse.copy_(s["lse"], non_blocking=True)
-        h_dqkv.copy_(s["dqkv"], non_blocking=True)
-    e1.record(stream)
+    down = (down0, down1)
+
+    def e2e_steps(n):
+        for c in cins + couts:
+            c.wait_stream(cs)
+        for i in range(n):
+            bi = i % 2
+            s = bufs[bi]
+            for k in range(2):
+                with torch.cuda.stream(cins[k]):
+                    if i >= 2:
+                        cins[k].wait_event(ev_comp[bi])  # step i-2 has read this set's inputs
+                    up[k](s)
+                    ev_in[k][bi].record(cins[k])
+                cs.wait_event(ev_in[k][bi])
+                if i >= 2:
+                    cs.wait_event(ev_out[k][bi])  # step i-2's results have left this set
+            for _, f in parts:
+                f(s, cs)
+            ev_comp[bi].record(cs)
+            for k in range(2):
+                with torch.cuda.stream(couts[k]):
+                    couts[k].wait_event(ev_comp[bi])
+                    down[k](s)
+                    ev_out[k][bi].record(couts[k])
+        for c in cins + couts:
+            cs.wait_stream(c)
+
+    barrier()
+    with torch.cuda.stream(cs):
+        e2e_steps(4)  # warm-up outside any graph
     torch.cuda.synchronize()
+    e2e_mode = "cuda-graph"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            e2e_steps(Ke)
+        run_e2e = graph.replay
+    except Exception as exc:  # capture unavailable: same sequence, launched eagerly
+        e2e_mode = f"eager ({type(exc).__name__})"
+        torch.cuda.synchronize()
+
+        def run_e2e():
+            with torch.cuda.stream(cs):
+                e2e_steps(Ke)
+    run_e2e()  # warm replay
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    with torch.cuda.stream(cs):
+        run_e2e()
+    e1.record(cs)
+    torch.cuda.synchronize()
+    if B.psa_get_last_device_error() != 0:
+        raise RuntimeError("device error during the end-to-end run")
     ms_e2e = e0.elapsed_time(e1)
     if dist is not None:
         t = torch.tensor([ms_e2e], device="cuda")
@@ -319,7 +384,9 @@ def run_ours(args, rank, world, local_rank):
         "kernel_us": {k: v * 1e3 for k, v in per.items()},
         "roofline": roof,
         "e2e": {"value": tokens_per_step * world * Ke / (ms_e2e / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+                "pipelining": "H2D of step i+1 and D2H of step i-1 overlap step i",
+                "launch": e2e_mode},
         "gpu_launches": launches_per_step * K,
         "clocks": sampler.summary(),
     }
