@@ -10,6 +10,11 @@ over one batch of the 'psa_fwdbwd_n400' workload: B=64, num_heads=4, KEY_DIM=32,
 --split-bwd times the two-kernel backward instead (psa_attention_bwd_dq then
 psa_attention_bwd_dkdv), the form that long sequences use.
 
+--sweep times the compute-bound cases instead, one JSON line each: the raw
+FlashAttention-2 calls over BH=64, N in {1024, 4096, 16384}, d in {32, 64}
+(forward, and dQ + dK/dV backward) and the N=1600 PSA step (B=32, 8 heads,
+40x40), as TFLOP/s and as a fraction of the bf16 tensor peak.
+
 --impl reference times the fp64 CPU oracle (the test oracle, untuned) on the
 host cores, on a bounded sample of the same workload per step.
 
@@ -430,6 +435,122 @@ def cpu_baseline(w, scale, budget_s=15.0, batches=None):
                       f"fp64 forward + backward, {t:.2f} s"}
 
 
+# ----------------------------------------------------------------------------- sweep
+def _time_loop(torch, fn, iters, warmup):
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters * 1e-3  # seconds per call
+
+
+def run_sweep(args):
+    """The long-sequence FA2 sweep and the N=1600 PSA step against the tensor peak.
+
+    FLOPs are the algorithmic ones: FA2 forward 4 BH N^2 d, backward 10 BH N^2 d
+    (S recomputed once); PSA step 192 N^2 + 448 N^2 per head (KD = 32).  The loops
+    run for seconds, so the fraction is taken against the sustained bf16 peak.
+    Inputs are seeded N(0,1) bf16 drawn on the device; enough input/output sets
+    rotate to exceed twice the L2 where one set is smaller than that.
+    """
+    import torch
+
+    from vision_transformer_attention_psapackqkv_gb300 import binding as B
+    from vision_transformer_attention_psapackqkv_gb300.inputs import (FA2_SWEEP_BH, FA2_SWEEP_D,
+                                                                      FA2_SWEEP_N, FA2_SWEEP_SEED,
+                                                                      PSA_WORKLOADS)
+
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(FA2_SWEEP_SEED)
+    rnd = lambda *shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    lines = []
+
+    def emit(workload, part, flops, sec, extra):
+        tf = flops / sec / 1e12
+        line = {"metric": "attention TFLOP/s (algorithmic FLOPs)", "workload": workload,
+                "part": part, "value": tf, "unit": "TFLOP/s", "us": sec * 1e6,
+                "higher_is_better": True, "dtype": "bf16", "flops": flops,
+                "tensor": {"peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                           "peak_source": f"{src}, sustained"}}
+        line.update(extra)
+        lines.append(line)
+        print(json.dumps(line), flush=True)
+
+    BH = FA2_SWEEP_BH
+    for d in FA2_SWEEP_D:
+        for N in FA2_SWEEP_N:
+            if args.case not in (None, f"fa2_bh{BH}_n{N}_d{d}"):
+                continue
+            shp = (BH, N, d)
+            per_set = 8 * BH * N * d * 2 + 2 * BH * N * 4
+            nsets = max(1, math.ceil(2 * 129e6 / per_set) + (1 if per_set < 2 * 129e6 else 0))
+            sets = []
+            for _ in range(nsets):
+                q, k, v, do = rnd(*shp), rnd(*shp), rnd(*shp), rnd(*shp)
+                sets.append({"q": q, "k": k, "v": v, "do": do, "o": torch.empty_like(q),
+                             "dq": torch.empty_like(q), "dk": torch.empty_like(q),
+                             "dv": torch.empty_like(q),
+                             "lse": torch.empty((BH, N), dtype=torch.float32, device="cuda"),
+                             "delta": torch.empty((BH, N), dtype=torch.float32, device="cuda")})
+            sc = 1.0 / math.sqrt(d)
+
+            def fwd(i):
+                s = sets[i % nsets]
+                B.flash_attn2_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], sc)
+
+            def bwd(i):
+                s = sets[i % nsets]
+                B.flash_attn2_bwd_dq(s["q"], s["k"], s["v"], s["o"], s["do"], s["lse"], s["delta"],
+                                     s["dq"], sc)
+                B.flash_attn2_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["lse"], s["delta"],
+                                       s["dk"], s["dv"], sc)
+
+            ff, fb = 4.0 * BH * N * N * d, 10.0 * BH * N * N * d
+            iters = max(5, min(400, int(3e13 / ff)))
+            with ClockSampler() as clk:
+                tfw = _time_loop(torch, fwd, iters, max(3, nsets))
+                tbw = _time_loop(torch, bwd, iters, max(3, nsets))
+            if B.psa_get_last_device_error() != 0:
+                raise RuntimeError("device error in the sweep")
+            extra = {"config": {"BH": BH, "N": N, "d": d, "iters": iters, "sets": nsets},
+                     "clocks": clk.summary()}
+            emit(f"fa2_bh{BH}_n{N}_d{d}", "fwd", ff, tfw, extra)
+            emit(f"fa2_bh{BH}_n{N}_d{d}", "bwd (dQ + dK/dV)", fb, tbw, extra)
+            del sets
+            torch.cuda.empty_cache()
+
+    w = PSA_WORKLOADS["psa_fwdbwd_n1600"]
+    if args.case not in (None, w.name):
+        return lines
+    qkv = rnd(w.B, w.qkv_channels, w.H, w.W)
+    dout = rnd(w.B, w.out_channels, w.H, w.W)
+    shape = B.shape_of(qkv, w.num_heads, w.key_dim)
+    sc = 1.0 / math.sqrt(w.key_dim)
+    out, vres, dqkv = torch.empty_like(dout), torch.empty_like(dout), torch.empty_like(qkv)
+    lse = torch.empty((w.BH, w.N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.psa_attention_bwd_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    pf = lambda i: B.psa_attention_fwd(qkv, out, lse, vres, shape, sc)
+    pb = lambda i: B.psa_attention_bwd(qkv, out, dout, lse, None, dqkv, ws, shape, sc)
+    n2 = float(w.N) * w.N * w.BH
+    with ClockSampler() as clk:
+        tpf = _time_loop(torch, pf, 100, 5)
+        tpb = _time_loop(torch, pb, 100, 5)
+    extra = {"config": {"B": w.B, "num_heads": w.num_heads, "key_dim": w.key_dim, "H": w.H,
+                        "W": w.W, "N": w.N, "iters": 100, "sets": 1},
+             "clocks": clk.summary()}
+    emit(w.name, "fwd", 192 * n2, tpf, extra)
+    emit(w.name, "bwd", 448 * n2, tpb, extra)
+    emit(w.name, "fwd+bwd", 640 * n2, tpf + tpb, extra)
+    return lines
+
+
 def run_reference(args):
     from vision_transformer_attention_psapackqkv_gb300.inputs import PSA_WORKLOADS
 
@@ -478,6 +599,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--split-bwd", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="with --sweep: run only the case of this name (e.g. fa2_bh64_n4096_d64)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -487,6 +611,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
         return
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:

@@ -98,8 +98,9 @@ RAGGED = [
     # (B, nh, KD, H, W): N = 8, 40, 136, 144 (KD = 64), 264, 72
     (1, 1, 32, 2, 4), (2, 3, 32, 5, 8), (1, 2, 32, 8, 17), (2, 1, 64, 12, 12), (1, 2, 32, 12, 22),
     (3, 2, 64, 8, 9),
-    # KD = 32 around the one-kernel backward's tiles and its limit: N = 128, 512, 520
-    (2, 1, 32, 8, 16), (1, 2, 32, 16, 32), (1, 1, 32, 4, 130),
+    # KD = 32 around the one-kernel backward's tiles and its limit: N = 128, 512, 520;
+    # around the single-pass forward's limit: N = 448, 456
+    (2, 1, 32, 8, 16), (1, 2, 32, 16, 32), (1, 1, 32, 4, 130), (1, 2, 32, 16, 28), (1, 1, 32, 8, 57),
 ]
 
 

@@ -107,27 +107,27 @@ __global__ void __launch_bounds__(128) psa_bwd_delta_kernel(const BwdArgs args) 
   }
 }
 // ---------------------------------------------------------------------- fused
-// P^T = 2^(s*sl2 - lse2[q]) (lse2 = +inf for queries >= N gives 0) and
-// dS^T = P^T (dP^T - delta[q]) of NC columns, packed to bf16 pairs.
+// P^T = 2^(s*sl2 - lse2[q]) and dS^T = P^T (dP^T - delta[q]) of NC columns,
+// packed to bf16 pairs.  The stats come negated (nlse2 = -lse2, -inf for
+// queries >= N, which gives P = 0; ndelta = -delta), so that every step is one
+// paired FP32 instruction for two columns.
 template <int NC>
 __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[NC], const uint32_t (&pv)[NC],
-                                           const float* lse2, const float* delta, float sl2,
+                                           const float* nlse2, const float* ndelta, float sl2,
                                            uint32_t* pw, uint32_t* dw) {
-  const float4* l4p = reinterpret_cast<const float4*>(lse2);
-  const float4* d4p = reinterpret_cast<const float4*>(delta);
+  const float2* l2p = reinterpret_cast<const float2*>(nlse2);
+  const float2* d2p = reinterpret_cast<const float2*>(ndelta);
+  const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-  for (int c = 0; c < NC; c += 4) {
-    const float4 l4 = l4p[c / 4], d4 = d4p[c / 4];
-    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-    const float p2 = fast_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-    const float p3 = fast_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
-    pw[c / 2] = pack_bf16x2(p0, p1);
-    pw[c / 2 + 1] = pack_bf16x2(p2, p3);
-    dw[c / 2] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - d4.x),
-                            p1 * (__uint_as_float(pv[c + 1]) - d4.y));
-    dw[c / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(pv[c + 2]) - d4.z),
-                                p3 * (__uint_as_float(pv[c + 3]) - d4.w));
+  for (int c = 0; c < NC; c += 2) {
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                sl2x2, l2p[c / 2]);
+    const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+    const float2 g =
+        __fadd2_rn(make_float2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), d2p[c / 2]);
+    const float2 ds = __fmul2_rn(p, g);
+    pw[c / 2] = pack_bf16x2(p.x, p.y);
+    dw[c / 2] = pack_bf16x2(ds.x, ds.y);
   }
 }
 
@@ -141,7 +141,7 @@ struct FusedCfg {
   static constexpr uint32_t STAGE_BYTES = Q_BYTES + DO_BYTES;
   static constexpr uint32_t HALF_BYTES = BK * 64 * 2;  // 128 keys x 64 queries, bf16
   static constexpr uint32_t PAIR_BYTES = 2 * HALF_BYTES;  // dS^T of a 128-query tile
-  static constexpr uint32_t HSTAT_BYTES = 2 * MAXN * 4;  // lse2[MAXN], delta[MAXN] of a head
+  static constexpr uint32_t HSTAT_BYTES = 2 * MAXN * 4;  // -lse2[MAXN], -delta[MAXN] of a head
   static constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + 2 * K_BYTES;
   static constexpr uint32_t OFF_STAGE = OFF_V + 2 * V_BYTES;
   static constexpr uint32_t OFF_PT = OFF_STAGE + ST * STAGE_BYTES;  // P^T: two buffers
@@ -230,9 +230,9 @@ __global__ void __launch_bounds__(608, 1)
 
   if (warp == C::kProducer) {
     // ------------------------------------------------------------ TMA producer
-    // K / V and Q / dO by lane 0.  The lse2 / delta of a whole head are written
-    // to shared memory by all lanes (double-buffered by head parity) from their
-    // registers (query lane + 32 i), which are loaded one head ahead, so no
+    // K / V and Q / dO by lane 0.  The negated lse2 / delta of a whole head are
+    // written to shared memory by all lanes (double-buffered by head parity) from
+    // their registers (query lane + 32 i), which are loaded one head ahead, so no
     // global-memory latency lands between two stages.
     bool ok = true;
     int kvc = 0, qc = 0;
@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(608, 1)
       for (int i = 0; i < kPer; ++i) {
         const int q = lane + 32 * i;
         const bool in = q < N;
-        nl[i] = in ? args.lse[(long long)bh * N + q] * kLog2e : INFINITY;
-        nd[i] = in ? args.delta[(long long)bh * N + q] : 0.f;
+        nl[i] = in ? -args.lse[(long long)bh * N + q] * kLog2e : -INFINITY;
+        nd[i] = in ? -args.delta[(long long)bh * N + q] : 0.f;
       }
     };
     if (nunits > 0) load_head(0);

@@ -117,28 +117,30 @@ __device__ __forceinline__ float softmax_row(uint32_t (&s)[NC], int valid, float
     alpha = fast_exp2(m_run - mx);
     m_run = mx;
   }
-  const float nm = -m_run;
-  float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+  // exponent arguments and the running sum two columns at a time (paired FP32
+  // instructions: half the issue slots of scalar FMA / add)
+  const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m_run, -m_run);
+  float2 l01 = make_float2(0.f, 0.f), l23 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < NC; c += 4) {
-    float p0 = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, nm));
-    float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 1]), sl2, nm));
-    float p2 = fast_exp2(fmaf(__uint_as_float(s[c + 2]), sl2, nm));
-    float p3 = fast_exp2(fmaf(__uint_as_float(s[c + 3]), sl2, nm));
+    const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
+                                  sl2x2, nm2);
+    const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])),
+                                  sl2x2, nm2);
+    float2 p01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
+    float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
     if (!kFull) {
-      p0 = c < valid ? p0 : 0.f;
-      p1 = c + 1 < valid ? p1 : 0.f;
-      p2 = c + 2 < valid ? p2 : 0.f;
-      p3 = c + 3 < valid ? p3 : 0.f;
+      p01.x = c < valid ? p01.x : 0.f;
+      p01.y = c + 1 < valid ? p01.y : 0.f;
+      p23.x = c + 2 < valid ? p23.x : 0.f;
+      p23.y = c + 3 < valid ? p23.y : 0.f;
     }
-    l0 += p0;
-    l1 += p1;
-    l2 += p2;
-    l3 += p3;
-    s[c / 2] = pack_bf16x2(p0, p1);
-    s[c / 2 + 1] = pack_bf16x2(p2, p3);
+    l01 = __fadd2_rn(l01, p01);
+    l23 = __fadd2_rn(l23, p23);
+    s[c / 2] = pack_bf16x2(p01.x, p01.y);
+    s[c / 2 + 1] = pack_bf16x2(p23.x, p23.y);
   }
-  l_run = l_run * alpha + ((l0 + l1) + (l2 + l3));
+  l_run = l_run * alpha + ((l01.x + l01.y) + (l23.x + l23.y));
   return alpha;
 }
 
