@@ -764,7 +764,7 @@ cudaError_t launch_fa2_bwd_dkdv(const CUtensorMap& mQ, const CUtensorMap& mK,
                                 const CUtensorMap& mV, const CUtensorMap& mDO,
                                 const BwdArgs& a, int BH, int d, cudaStream_t st) {
   (void)BH;
-  if (d == 32) return run_dkdv<32, 32, false, 2, 3, 2>(mQ, mK, mV, mDO, a, st);
+  if (d == 32) return run_dkdv<32, 32, false, 2, 4, 2>(mQ, mK, mV, mDO, a, st);
   return run_dkdv<64, 64, false, 1, 2, 2>(mQ, mK, mV, mDO, a, st);
 }
 
@@ -780,7 +780,7 @@ cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st) {
   (void)BH;
-  if (KD == 32) return run_dkdv<32, 64, true, 2, 2, 2>(mQK, mQK, mV, mDO, a, st);
+  if (KD == 32) return run_dkdv<32, 64, true, 1, 3, 2>(mQK, mQK, mV, mDO, a, st);
   return run_dkdv<64, 128, true, 2, 3, 1>(mQK, mQK, mV, mDO, a, st);
 }
 

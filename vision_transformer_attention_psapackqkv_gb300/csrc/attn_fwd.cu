@@ -627,7 +627,7 @@ cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
   // <DQK, DV, layout, slots per CTA, Q buffers, K/V stages>: two CTAs per SM, each
   // within half of the SM's shared memory and tensor memory
   if (d == 32) return launch_tc<32, 32, false, 1, 2, 4>(mQ, mK, mV, a, st);
-  return launch_tc<64, 64, false, 1, 2, 2>(mQ, mK, mV, a, st);
+  return launch_tc<64, 64, false, 1, 1, 3>(mQ, mK, mV, a, st);
 }
 
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
