@@ -18,6 +18,10 @@
 //                      registers, so it overlaps the exponentials of tile k.
 // The bf16 kernels run persistent grids; with one slot per CTA two CTAs share
 // an SM (and its tensor core), which interleaves their softmax and MMA phases.
+// Split rows (kSplit, short sequences): warps 0-3 and 4-7 both cover the 128 rows,
+// each thread owning one 32-key half of every tile with its own running max and
+// sum and its own O accumulator in TMEM (P.V k-steps of half h go to accumulator
+// h); the epilogue merges the halves, O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l.
 // Softmax: running max in the log2 domain; p = 2^(scale*log2e*s - m) rounded to
 // bf16 into P (K-major, 128-byte swizzle); O is rescaled in TMEM only when a row
 // max grows by more than 2^8 (exact either way, since O and the running sum
@@ -44,15 +48,21 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
 struct FwdCfg {
-  // 64-key tiles keep a whole S row in ~64 registers of its thread
+  // 64-key tiles keep a whole S row in ~64 registers of its thread; with kSplit
+  // two threads share a query row, each owning one 32-key half of every tile
+  // with its own running max / sum and its own O accumulator
   static constexpr int BM = 128, BN = 64, STAGES = ST;
   static_assert(ST >= 2 && ST <= 4 && QBUF >= 1 && QBUF <= 2, "buffering");
-  static constexpr int kSoftmaxWarps = 4 * NWG;
+  static_assert(!kSplit || NWG == 1, "split rows run one slot per CTA");
+  static constexpr int H = kSplit ? 2 : 1;  // softmax threads per query row
+  static constexpr int HC = BN / H;         // S columns per softmax thread
+  static constexpr int kRowThreads = 128 * H;  // softmax threads of a slot
+  static constexpr int kSoftmaxWarps = 4 * NWG * H;
   // control warps: TMA producer, MMA issuer (TMEM owner)
-  static constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1;
-  static constexpr int kThreads = 128 * NWG + 64;
+  static constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;
   static constexpr uint32_t Q_BYTES = BM * DQK * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2;
   static constexpr uint32_t V_BYTES = BN * DV * 2;
@@ -62,12 +72,16 @@ struct FwdCfg {
   static constexpr uint32_t SL_K = SL_Q + QBUF * Q_BYTES;
   static constexpr uint32_t SL_V = SL_K + STAGES * K_BYTES;
   static constexpr uint32_t SL_P = SL_V + STAGES * V_BYTES;
-  static constexpr uint32_t SL_BYTES = SL_P + 2 * P_BYTES;  // P double-buffered
+  // split rows: per tile parity, (max, sum) of both halves of every row
+  static constexpr uint32_t SL_ML = SL_P + 2 * P_BYTES;  // P double-buffered
+  static constexpr uint32_t SL_BYTES = SL_ML + (kSplit ? 2 * 2 * BM * 8 : 0);
   static constexpr uint32_t OFF_BAR = NWG * SL_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
-  // tensor memory per slot w: S (BN columns) at TM_SLOT * w, O (DV columns) after it
+  // tensor memory per slot w: S (BN columns) at TM_SLOT * w, then H O accumulators
+  // (DV columns each; accumulator h sums the P.V products of key half h)
   static constexpr uint32_t TM_O = BN;
-  static constexpr uint32_t TM_SLOT = (BN + DV <= 128) ? 128 : 256;
+  static constexpr uint32_t TM_SLOT = (BN + H * DV <= 128) ? 128 : 256;
+  static_assert(BN + H * DV <= 256, "tensor memory per slot");
   static constexpr uint32_t TMEM_COLS = NWG * TM_SLOT < 32 ? 32 : NWG * TM_SLOT;
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(DQK % 16 == 0 && DV % 32 == 0 && DV <= 128, "tile shape");
@@ -78,6 +92,7 @@ struct FwdCfg {
 struct SlotBars {
   uint64_t q_full[2], q_empty[2], kv_full[4], kv_empty[4];
   uint64_t s_full, s_free, p_full[2], pv_done[2], o_free;  // P / P.V per P buffer
+  uint64_t ml_ready;  // split rows: both halves' (max, sum) of the tile are in shared memory
 };
 
 // Loads this thread's NC-column S row from TMEM into registers with a single
@@ -149,12 +164,12 @@ __device__ __forceinline__ int slot_tiles(int slot, int nslots, int T) {
   return slot < T ? (T - slot + nslots - 1) / nslots : 0;
 }
 
-template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
-__global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
+__global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 2 : 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQK,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST>;
+  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t sbase = smem_addr(smem);
@@ -182,12 +197,13 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
         mbar_init(&b.kv_empty[i], 1);
       }
       mbar_init(&b.s_full, 1);
-      mbar_init(&b.s_free, 128);
+      mbar_init(&b.s_free, C::kRowThreads);
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&b.p_full[i], 128);
+        mbar_init(&b.p_full[i], C::kRowThreads);
         mbar_init(&b.pv_done[i], 1);
       }
-      mbar_init(&b.o_free, 128);
+      mbar_init(&b.o_free, C::kRowThreads);
+      mbar_init(&b.ml_ready, C::kRowThreads);
     }
     mbar_init(mma_done, 1);
     *abort = 0;
@@ -333,13 +349,17 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
         const uint64_t dV = dV0 + slot_off + (uint64_t)((k % C::STAGES) * C::V_BYTES >> 4);
         const uint32_t tO = tmem + w * C::TM_SLOT + C::TM_O;
         const int valid = min(C::BN, N - j * C::BN);
+        // k-steps of key half h accumulate into O accumulator h
+        constexpr int KH = C::HC / 16;
         if (valid == C::BN) {
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_bf16(tO, dP + kk * kStepP, dV + kk * kStepV, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tO + (kk / KH) * DV, dP + kk * kStepP, dV + kk * kStepV, idPV,
+                     (j > 0 || kk % KH > 0) ? 1u : 0u);
         } else {
           for (int kk = 0; kk * 16 < valid; ++kk)
-            mma_bf16(tO, dP + kk * kStepP, dV + kk * kStepV, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tO + (kk / KH) * DV, dP + kk * kStepP, dV + kk * kStepV, idPV,
+                     (j > 0 || kk % KH > 0) ? 1u : 0u);
         }
         mma_commit(&b.pv_done[k & 1]);
         mma_commit(&b.kv_empty[k % C::STAGES]);
@@ -363,11 +383,14 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
   }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int w = warp >> 2;               // slot
-    const int r = threadIdx.x - 128 * w;   // query row within the tile = TMEM lane
-    const int wq = warp & 3;               // warp within the slot
+    const int w = kSplit ? 0 : warp >> 2;  // slot
+    const int h = kSplit ? warp >> 2 : 0;  // key half of every tile this thread owns
+    const int wq = warp & 3;               // TMEM lane quadrant
+    const int r = wq * 32 + lane;          // query row within the tile = TMEM lane
+    const int tid = h * 128 + r;           // softmax thread within the slot
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + w * C::TM_SLOT, tO = tS + C::TM_O;
+    // S, and the O accumulator of this thread's key half
+    const uint32_t tS = tmem + w * C::TM_SLOT, tO = tS + C::TM_O + h * DV;
     const uint32_t sl = sbase + w * C::SL_BYTES;
     SlotBars& b = bars[w];
     const float sl2 = args.scale_log2;
@@ -381,7 +404,9 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
       for (int j = 0; j < nkv; ++j) {
         const int k = i * nkv + j;
         const int valid = min(C::BN, N - j * C::BN);
-        const int kend = (valid + 15) & ~15;
+        // valid columns of this thread's half, and the columns the products wrote
+        const int vh = min(max(valid - h * C::HC, 0), C::HC);
+        const int kend = (vh + 15) & ~15;
         if (!mbar_wait(&b.s_full, k & 1, abort)) {
           ok = false;
           break;
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
           }
           constexpr int kBoxes = C::BN / 64;
           const uint32_t vb = sl + C::SL_V + (k % C::STAGES) * C::V_BYTES;
-          for (int e = r; e < DV * kBoxes; e += 128) {
+          for (int e = tid; e < DV * kBoxes; e += C::kRowThreads) {
             const int ch = e / kBoxes, box = e % kBoxes;
             const int pos0 = j * C::BN + box * 64;
             __nv_bfloat16* dst = args.vres +
@@ -415,16 +440,17 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
             }
           }
         }
-        // the whole S row goes to registers at once, so the S buffer is handed back
-        // to the MMA warp (which starts S_{k+1}) before the exponentials
-        uint32_t s[C::BN];
-        if (active) load_s_row(tS + lane_base, kend, s);
+        // this thread's part of the S row goes to registers at once, so the S buffer
+        // is handed back to the MMA warp (which starts S_{k+1}) before the
+        // exponentials
+        uint32_t s[C::HC];
+        if (active && kend > 0) load_s_row(tS + lane_base + h * C::HC, kend, s);
         tc_fence_before();
         mbar_arrive(&b.s_free);
         float alpha = 1.f;
         if (active)
-          alpha = valid == C::BN ? softmax_row<true, C::BN>(s, valid, sl2, j == 0, m_run, l_run)
-                                 : softmax_row<false, C::BN>(s, valid, sl2, j == 0, m_run, l_run);
+          alpha = vh == C::HC ? softmax_row<true, C::HC>(s, vh, sl2, j == 0, m_run, l_run)
+                              : softmax_row<false, C::HC>(s, vh, sl2, j == 0, m_run, l_run);
         // P buffer k & 1 was last read by P.V of k - 2
         if (k >= 2 && !mbar_wait(&b.pv_done[k & 1], ((k >> 1) - 1) & 1, abort)) {
           ok = false;
@@ -434,10 +460,12 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
         if (active) {
           const uint32_t pbuf = sl + C::SL_P + (k & 1) * C::P_BYTES;
 #pragma unroll
-          for (int ch = 0; ch < C::BN / 8; ++ch)
+          for (int ch = 0; ch < C::HC / 8; ++ch) {
+            const int gch = h * (C::HC / 8) + ch;  // 16-byte chunk within the P row
             if (ch * 8 < kend)
-              st_shared_v4(pbuf + (ch >> 3) * (C::BM * 128) + swizzled_offset(r, ch & 7, 128),
+              st_shared_v4(pbuf + (gch >> 3) * (C::BM * 128) + swizzled_offset(r, gch & 7, 128),
                            s[ch * 4], s[ch * 4 + 1], s[ch * 4 + 2], s[ch * 4 + 3]);
+          }
           // O may only be rescaled once every earlier P.V has landed in it
           if (__any_sync(0xffffffffu, alpha != 1.f) &&
               !mbar_wait(&b.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort)) {
@@ -446,7 +474,7 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
           }
           tc_fence_after();
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < DV; c += 32) {
               float o[32];
               tmem_load32(tO + lane_base + c, o);
@@ -468,7 +496,61 @@ __global__ void __launch_bounds__(128 * NWG + 64, NWG == 1 ? 2 : 1)
         break;
       }
       tc_fence_after();
-      if (active) {
+      if (kSplit) {
+        // both halves' (max, sum) of the row, then this thread writes channels
+        // [h * DV/2, (h + 1) * DV/2) of O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l
+        float* ml = reinterpret_cast<float*>(smem + w * C::SL_BYTES + C::SL_ML) + (i & 1) * 512;
+        ml[h * 256 + 2 * r] = m_run;
+        ml[h * 256 + 2 * r + 1] = l_run;
+        mbar_arrive(&b.ml_ready);
+        if (!mbar_wait(&b.ml_ready, i & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const float m0 = ml[2 * r], l0 = ml[2 * r + 1];
+        const float m1 = ml[256 + 2 * r], l1 = ml[256 + 2 * r + 1];
+        // a half without any valid key (N <= 32) has l = 0 and an unwritten accumulator
+        const float mx = l1 > 0.f ? fmaxf(m0, m1) : m0;
+        const float f0 = fast_exp2(m0 - mx), f1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
+        const float l = l0 * f0 + l1 * f1;
+        const float c0s = f0 / l, c1s = f1 / l;
+        if (active) {
+          const int q = q0 + r;
+          const bool live = q < N;
+#pragma unroll 1
+          for (int c = 0; c < DV / 2; c += 16) {
+            const int ch = h * (DV / 2) + c;
+            uint32_t a0[16], a1[16];
+            tmem_load16_async(tS + C::TM_O + lane_base + ch, a0);
+            tmem_load16_async(tS + C::TM_O + DV + lane_base + ch, a1);
+            tmem_wait_ld();
+            tmem_pin(a0);
+            tmem_pin(a1);
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[e] = l1 > 0.f ? __uint_as_float(a0[e]) * c0s + __uint_as_float(a1[e]) * c1s
+                              : __uint_as_float(a0[e]) * c0s;
+            if (live) {
+              if (kNCHW) {
+                __nv_bfloat16* dst = args.out +
+                    ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + ch) * N + q;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dst[(long long)e * N] = __float2bfloat16_rn(o[e]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + ch);
+#pragma unroll
+                for (int e = 0; e < 16; e += 8)
+                  dst[e / 8] = make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
+                                          pack_bf16x2(o[e + 4], o[e + 5]),
+                                          pack_bf16x2(o[e + 6], o[e + 7]));
+              }
+            }
+          }
+          if (h == 0 && live && args.lse)
+            args.lse[(long long)bh * N + q] = (mx + log2f(l)) * kLn2;
+        }
+      } else if (active) {
         const float inv_l = 1.f / l_run;
         const int q = q0 + r;
         const bool live = q < N;
@@ -592,11 +674,11 @@ int sm_count() {
   return n;
 }
 
-template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST>
+template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
 cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUtensorMap& mV,
                       const FwdArgs& a, cudaStream_t st) {
-  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST>;
-  auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW, NWG, QBUF, ST>;
+  using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
+  auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
@@ -624,16 +706,22 @@ cudaError_t launch_f32(const float* q, const float* k, const float* v, float* ou
 cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
                                 const CUtensorMap& mV, const FwdArgs& a, int d,
                                 cudaStream_t st) {
-  // <DQK, DV, layout, slots per CTA, Q buffers, K/V stages>: two CTAs per SM, each
-  // within half of the SM's shared memory and tensor memory
-  if (d == 32) return launch_tc<32, 32, false, 1, 2, 4>(mQ, mK, mV, a, st);
-  return launch_tc<64, 64, false, 1, 1, 3>(mQ, mK, mV, a, st);
+  // <DQK, DV, layout, slots per CTA, Q buffers, K/V stages, split rows>: two CTAs
+  // per SM, each within half of the SM's shared memory and tensor memory
+  // (split rows measured slower on long sequences: the hand-off chain between the
+  // row threads and the MMA warp, not the per-row exponentials, sets their pace)
+  if (d == 32) return launch_tc<32, 32, false, 1, 2, 4, false>(mQ, mK, mV, a, st);
+  return launch_tc<64, 64, false, 1, 1, 3, false>(mQ, mK, mV, a, st);
 }
 
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const FwdArgs& a, int KD, cudaStream_t st) {
-  if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4>(mQK, mQK, mV, a, st);
-  return launch_tc<64, 128, true, 1, 1, 2>(mQK, mQK, mV, a, st);
+  // split rows for the short sequences of vision feature maps (N = 400: 41.7 against
+  // 42.7 us), one thread per row beyond (N = 1600: 267 against 291 us)
+  if (KD == 32 && a.N <= 512) return launch_tc<32, 64, true, 1, 2, 4, true>(mQK, mQK, mV, a, st);
+  if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4, false>(mQK, mQK, mV, a, st);
+  // DV = 128: two accumulators would not leave room for a second CTA's tensor memory
+  return launch_tc<64, 128, true, 1, 1, 2, false>(mQK, mQK, mV, a, st);
 }
 
 cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
