@@ -33,6 +33,26 @@ cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, 
                                int N, float scale, cudaStream_t st);
 
 // Multiprocessor count of the current device (queried once; persistent grids).
+// Launches kern with programmatic stream serialization: its CTAs may become
+// resident and run their prologue (barrier set-up, tensor memory allocation)
+// while the previous kernel of the stream finishes; the kernels call pdl_wait()
+// before their first global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 inline int device_sm_count() {
   static const int n = [] {
     int dev = 0, v = 0;

@@ -133,6 +133,10 @@ __global__ void __launch_bounds__(192, CPS)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done: the next kernel may start its own; the previous one must have
+  // finished before this grid reads or writes global memory
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -455,6 +459,10 @@ __global__ void __launch_bounds__(192, CPS)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done: the next kernel may start its own; the previous one must have
+  // finished before this grid reads or writes global memory
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 4) {
     // producer: K/V per unit by TMA; per query tile Q, dO by TMA and lse / delta by
@@ -728,8 +736,8 @@ cudaError_t launch(K kern, const BwdArgs& a, int rows_per_unit, cudaStream_t st,
   if (attr != cudaSuccess) return attr;
   const long long units = (long long)a.BH * ((a.N + rows_per_unit - 1) / rows_per_unit);
   const long long ctas = std::min<long long>((long long)CPS * device_sm_count(), units);
-  kern<<<(unsigned)ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(maps..., a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st,
+                    maps..., a);
 }
 
 // <DQK, DV, layout, Q or K/V buffers, stages, CTAs per SM>

@@ -64,6 +64,8 @@ __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162f
 template <int DV>
 __global__ void __launch_bounds__(128) psa_bwd_delta_kernel(const BwdArgs args) {
   static_assert(DV == 64, "eight slices of eight channels");
+  pdl_launch_dependents();
+  pdl_wait();  // Out / dOut come from earlier kernels of the stream
   const int N = args.N;
   const int wpr = (N + 31) / 32;  // warps per head
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -227,6 +229,10 @@ __global__ void __launch_bounds__(608, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done: the next kernel may start its own; the previous one must have
+  // finished before this grid reads or writes global memory
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == C::kProducer) {
     // ------------------------------------------------------------ TMA producer
@@ -552,8 +558,8 @@ cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
   if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.delta)
     return cudaErrorInvalidValue;
   const long long warps = (long long)a.BH * ((a.N + 31) / 32);
-  psa_bwd_delta_kernel<64><<<(unsigned)((warps * 32 + 127) / 128), 128, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(psa_bwd_delta_kernel<64>, dim3((unsigned)((warps * 32 + 127) / 128)),
+                             dim3(128), 0, st, a);
   if (e != cudaSuccess) return e;
   using Cfg = FusedCfg<32, 64, 4>;
   auto kern = attn_bwd_fused_kernel<32, 64, 4>;
@@ -561,8 +567,8 @@ cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   const int ctas = std::min(device_sm_count(), a.BH);
-  kern<<<ctas, Cfg::kThreads, Cfg::SMEM_BYTES, st>>>(mQK, mQK, mV, mDO, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st, mQK, mQK, mV,
+                    mDO, a);
 }
 
 }  // namespace psa

@@ -217,6 +217,10 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done: the next kernel may start its own; the previous one must have
+  // finished before this grid reads or writes global memory
+  pdl_launch_dependents();
+  pdl_wait();
 
   int ntiles[NWG];
   int max_tiles = 0;
@@ -686,8 +690,8 @@ cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUten
   const long long T = (long long)a.BH * ((a.N + C::BM - 1) / C::BM);
   const long long per_sm = NWG == 1 ? 2 : 1;
   const long long ctas = std::min<long long>(per_sm * sm_count(), (T + NWG - 1) / NWG);
-  kern<<<(unsigned)ctas, C::kThreads, C::SMEM_BYTES, st>>>(mQK, mK, mV, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)ctas), dim3(C::kThreads), C::SMEM_BYTES, st, mQK, mK,
+                    mV, a);
 }
 
 template <int DQK, int DV, bool kNCHW>

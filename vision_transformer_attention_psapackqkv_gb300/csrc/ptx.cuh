@@ -121,6 +121,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Programmatic dependent launch.  pdl_launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) start its CTAs
+// once every CTA of this grid has signalled or exited; pdl_wait blocks until the
+// previous kernel of the stream has completed and its memory writes are visible
+// (it returns at once for a kernel launched without the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tcgen05.mma operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
