@@ -95,6 +95,24 @@ def work_model(w):
     return k, step
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value, dist=None, device=None):
+    """A per-rank float reduced to its maximum over all ranks (the job takes as long
+    as its slowest replica); unchanged on a single process."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step, world, steps, ms):
+    """Whole-job throughput: the units every replica processed over the job's time."""
+    return units_per_step * world * steps / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock and clock-event reasons through NVML (read-only) in a thread."""
@@ -255,10 +273,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
            for j, (name, _) in enumerate(parts)}
-    if dist is not None:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, "cuda")
     if B.psa_get_last_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -350,11 +365,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if B.psa_get_last_device_error() != 0:
         raise RuntimeError("device error during the end-to-end run")
-    ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     h2d = h_qkv.numel() * 2 + h_dout.numel() * 2
     d2h = h_out.numel() * 2 * 2 + h_lse.numel() * 4 + h_dqkv.numel() * 2
 
@@ -362,8 +373,8 @@ def run_ours(args, rank, world, local_rank):
     kmodel, step_model = work_model(w)
     peaks, peak_src = load_peaks()
     ms_step = ms_total / K
-    value = tokens_per_step * world * K / (ms_total / 1e3)
-    tflops = step_model["flops"] * world * K / (ms_total / 1e3) / 1e12
+    value = job_throughput(tokens_per_step, world, K, ms_total)
+    tflops = job_throughput(step_model["flops"], world, K, ms_total) / 1e12
     # the dominant kernel (largest time share) and its roofline
     dom = max(per, key=per.get)
     km = kmodel[dom]
@@ -397,7 +408,7 @@ def run_ours(args, rank, world, local_rank):
                           "peak_source": peak_src},
         "kernel_us": {k: v * 1e3 for k, v in per.items()},
         "roofline": roof,
-        "e2e": {"value": tokens_per_step * world * Ke / (ms_e2e / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens_per_step, world, Ke, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "pipelining": "H2D of step i+1 and D2H of step i-1 overlap step i",
                 "launch": e2e_mode},
