@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per call of each step part, measured with ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum) on this workload for the current
 # kernels; to be re-measured whenever a kernel changes.
-MEASURED_TRAFFIC = {"fwd": 26.26e6 + 0.006e6, "bwd": 26.23e6 + 40.19e6 + 0.91e6,
+MEASURED_TRAFFIC = {"fwd": 26.26e6 + 0.006e6, "bwd": 52.90e6 + 1.51e6,
                     "bwd_dq": 52.88e6 + 0.33e6, "bwd_dkdv": 40.21e6 + 0.30e6}
 
 
@@ -229,8 +229,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         parts = (("fwd", fwd), ("bwd", bwd))
     # kernels per call: the forward (PsaExtractV fused) 1; psa_attention_bwd at this
-    # sequence length 2 (delta pass + one-kernel backward); dQ 1; dK/dV 1
-    launches = {"fwd": 1, "bwd": 2, "bwd_dq": 1, "bwd_dkdv": 1}
+    # sequence length 1 (one kernel per head, delta included); dQ 1; dK/dV 1
+    launches = {"fwd": 1, "bwd": 1, "bwd_dq": 1, "bwd_dkdv": 1}
     launches_per_step = sum(launches[name] for name, _ in parts)
 
     def barrier():

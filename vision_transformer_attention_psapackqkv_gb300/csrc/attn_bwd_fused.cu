@@ -12,8 +12,9 @@
 // head stays in tensor memory for the whole walk (4 x 32 columns), which is
 // what bounds N.
 //
-// Two launches: psa_bwd_delta_kernel writes delta = rowsum(dO o O) (a
-// bandwidth-bound pass over Out and dOut), then the fused kernel.
+// One launch: at the start of each head the row threads compute the head's
+// delta = rowsum(dO o O) from Out and dOut (while the head's first tiles load),
+// so no separate pass over Out and dOut runs and delta never leaves the SM.
 //
 // Layout: QKV / Out / dOut in NCHW, dQKV written in NCHW (the adjoints of
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing, the optional
@@ -28,8 +29,8 @@
 //              exponentials); they turn S^T / dP^T into bf16 P^T and dS^T in
 //              shared memory and write dK, dV per key tile and dQ per head;
 //   warp 16    TMA producer (K / V per key tile, double-buffered; Q / dO per step
-//              in a ring; lse2 / delta of a head into shared memory, from
-//              registers loaded one head ahead);
+//              in a ring; lse2 of a head into shared memory, from registers
+//              loaded one head ahead);
 //   warp 17    issues S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffers
 //              (64 + 64 columns each, by step parity) and owns the 512 columns;
 //   warp 18    issues the gradient products into dV (64 columns), dK (32) and
@@ -56,58 +57,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
 
-// ---------------------------------------------------------------------- delta
-// delta[bh, q] = sum_c Out[b, head c, q] * dOut[b, head c, q] over the DV output
-// channels of head bh (NCHW, positions contiguous).  A warp covers 32 positions of
-// one head: lane = 8-channel slice (lane / 4) x 8-position group (lane % 4); the
-// eight slices are summed with shuffles.  N is a multiple of 8.
-template <int DV>
-__global__ void __launch_bounds__(128) psa_bwd_delta_kernel(const BwdArgs args) {
-  static_assert(DV == 64, "eight slices of eight channels");
-  pdl_launch_dependents();
-  pdl_wait();  // Out / dOut come from earlier kernels of the stream
-  const int N = args.N;
-  const int wpr = (N + 31) / 32;  // warps per head
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (gw >= (long long)args.BH * wpr) return;  // whole warps only
-  const int lane = threadIdx.x & 31;
-  const int bh = (int)(gw / wpr);
-  const int q0 = (int)(gw % wpr) * 32 + (lane & 3) * 8;
-  const int c0 = (lane >> 2) * 8;
-  const bool in = q0 < N;
-  const long long row = (long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + c0;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (in) {
-    uint4 ov[8], gv[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      ov[c] = *reinterpret_cast<const uint4*>(args.o + (row + c) * N + q0);
-      gv[c] = *reinterpret_cast<const uint4*>(args.dO + (row + c) * N + q0);
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[c]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[c]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
-        acc[2 * e] = fmaf(of.x, gf.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(of.y, gf.y, acc[2 * e + 1]);
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 4);
-    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 8);
-    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
-  }
-  if (in && (lane >> 2) == 0) {
-    float4* d = reinterpret_cast<float4*>(args.delta + (long long)bh * N + q0);
-    d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  }
-}
 // ---------------------------------------------------------------------- fused
 // P^T = 2^(s*sl2 - lse2[q]) and dS^T = P^T (dP^T - delta[q]) of NC columns,
 // packed to bf16 pairs.  The stats come negated (nlse2 = -lse2, -inf for
@@ -163,6 +112,7 @@ struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[8], q_empty[8];
   uint64_t s_full[2], s_free[2], p_full[2], g_done[2], hs_full[2], hs_free[2];
   uint64_t acc_full, acc_free, mma_done[2];
+  uint64_t dl_part, dl_full;  // a head's delta: partial sums written, delta written
 };
 static_assert(sizeof(FusedBars) + 8 <= 512, "barrier area");
 
@@ -218,6 +168,8 @@ __global__ void __launch_bounds__(608, 1)
     }
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.acc_free, 32 * C::kRowWarps);
+    mbar_init(&b.dl_part, 32 * C::kRowWarps);
+    mbar_init(&b.dl_full, 32 * C::kRowWarps);
     *abort = 0;
     fence_mbar_init();
   }
@@ -236,22 +188,21 @@ __global__ void __launch_bounds__(608, 1)
 
   if (warp == C::kProducer) {
     // ------------------------------------------------------------ TMA producer
-    // K / V and Q / dO by lane 0.  The negated lse2 / delta of a whole head are
-    // written to shared memory by all lanes (double-buffered by head parity) from
-    // their registers (query lane + 32 i), which are loaded one head ahead, so no
-    // global-memory latency lands between two stages.
+    // K / V and Q / dO by lane 0.  The negated lse2 of a whole head is written to
+    // shared memory by all lanes (double-buffered by head parity) from their
+    // registers (query lane + 32 i), which are loaded one head ahead, so no
+    // global-memory latency lands between two stages.  (The row threads add the
+    // head's delta.)
     bool ok = true;
     int kvc = 0, qc = 0;
     constexpr int kPer = C::MAXN / 32;
-    float nl[kPer], nd[kPer];
+    float nl[kPer];
     auto load_head = [&](int u) {
       const int bh = head_of(u);
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const int q = lane + 32 * i;
-        const bool in = q < N;
-        nl[i] = in ? -args.lse[(long long)bh * N + q] * kLog2e : -INFINITY;
-        nd[i] = in ? -args.delta[(long long)bh * N + q] : 0.f;
+        nl[i] = q < N ? -args.lse[(long long)bh * N + q] * kLog2e : -INFINITY;
       }
     };
     if (nunits > 0) load_head(0);
@@ -263,10 +214,7 @@ __global__ void __launch_bounds__(608, 1)
       }
       float* hst = reinterpret_cast<float*>(smem + C::OFF_HSTAT + (u & 1) * C::HSTAT_BYTES);
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        hst[lane + 32 * i] = nl[i];
-        hst[C::MAXN + lane + 32 * i] = nd[i];
-      }
+      for (int i = 0; i < kPer; ++i) hst[lane + 32 * i] = nl[i];
       mbar_arrive(&b.hs_full[u & 1]);
       if (u + 1 < nunits) load_head(u + 1);
       for (int kt = 0; ok && kt < nkt; ++kt) {
@@ -417,11 +365,62 @@ __global__ void __launch_bounds__(608, 1)
     bool ok = true;
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
+      float* hst = reinterpret_cast<float*>(smem + C::OFF_HSTAT + (u & 1) * C::HSTAT_BYTES);
+      {
+        // delta[q] = sum_c Out[c, q] dOut[c, q] over the head's DV channels, while
+        // its first tiles load.  Thread t = 64 s + g sums channels 8s .. 8s+7 at
+        // positions 8g .. 8g+7; the eight channel slices meet in the P^T buffers,
+        // idle here (every product of the previous head has completed: its last
+        // dV / dK epilogue waited for them).
+        static_assert(C::kRowWarps * 32 == C::MAXN && DV == 64, "one thread per 8 x 8 block");
+        const int t = threadIdx.x, g = t & 63, sl8 = t >> 6;
+        float part[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[e] = 0.f;
+        if (8 * g < N) {
+          const long long base = ((long long)out_row(bh) + 8 * sl8) * N + 8 * g;
+          uint4 ov[8], dv[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            ov[c] = __ldg(reinterpret_cast<const uint4*>(args.o + base + (long long)c * N));
+            dv[c] = __ldg(reinterpret_cast<const uint4*>(args.dO + base + (long long)c * N));
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t ow[4] = {ov[c].x, ov[c].y, ov[c].z, ov[c].w};
+            const uint32_t dw4[4] = {dv[c].x, dv[c].y, dv[c].z, dv[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 o2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+              const float2 d2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw4[e]));
+              part[2 * e] = fmaf(o2.x, d2.x, part[2 * e]);
+              part[2 * e + 1] = fmaf(o2.y, d2.y, part[2 * e + 1]);
+            }
+          }
+        }
+        float* scratch = reinterpret_cast<float*>(smem + C::OFF_PT);
+        float4* sp = reinterpret_cast<float4*>(scratch + sl8 * C::MAXN + 8 * g);
+        sp[0] = make_float4(part[0], part[1], part[2], part[3]);
+        sp[1] = make_float4(part[4], part[5], part[6], part[7]);
+        mbar_arrive(&b.dl_part);
+        if (!mbar_wait(&b.dl_part, u & 1, abort)) {
+          ok = false;
+          break;
+        }
+        float dsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dsum += scratch[k * C::MAXN + t];
+        hst[C::MAXN + t] = t < N ? -dsum : 0.f;
+        mbar_arrive(&b.dl_full);
+        if (!mbar_wait(&b.dl_full, u & 1, abort)) {
+          ok = false;
+          break;
+        }
+      }
       if (!mbar_wait(&b.hs_full[u & 1], (u >> 1) & 1, abort)) {
         ok = false;
         break;
       }
-      const float* hst = reinterpret_cast<const float*>(smem + C::OFF_HSTAT + (u & 1) * C::HSTAT_BYTES);
       for (int kt = 0; ok && kt < nkt; ++kt) {
         const int kvi = u * nkt + kt;
         const int vk = min(C::BK, N - kt * C::BK);
@@ -555,12 +554,8 @@ __global__ void __launch_bounds__(608, 1)
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
                                  const CUtensorMap& mDO, const BwdArgs& a, int KD,
                                  cudaStream_t st) {
-  if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.delta)
+  if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.o || !a.dO)
     return cudaErrorInvalidValue;
-  const long long warps = (long long)a.BH * ((a.N + 31) / 32);
-  cudaError_t e = launch_pdl(psa_bwd_delta_kernel<64>, dim3((unsigned)((warps * 32 + 127) / 128)),
-                             dim3(128), 0, st, a);
-  if (e != cudaSuccess) return e;
   using Cfg = FusedCfg<32, 64, 4>;
   auto kern = attn_bwd_fused_kernel<32, 64, 4>;
   static const cudaError_t attr =
