@@ -33,6 +33,11 @@
  *   - Kernels that wait on on-chip barriers give up after a bounded time and
  *     record PSA_ERR_TIMEOUT in a device-side error word that
  *     psa_get_last_device_error() reads and clears.
+ *   - The attention kernels are launched with programmatic stream
+ *     serialization: their CTAs may start their set-up while the previous
+ *     kernel of the stream is finishing, but they read and write no global
+ *     memory before that kernel has completed, so results are exactly those of
+ *     plain stream order.
  */
 #ifndef PSA_GB300_H
 #define PSA_GB300_H
@@ -129,8 +134,9 @@ psa_status_t psa_attention_fwd(const void *qkv_nchw, void *out_nchw, float *lse,
  * upstream gradient dout [B, c, H, W] and optionally the gradient dvres of the
  * extracted V (nullable), writes dqkv_nchw [B, qkv_h, H, W] (overwritten, V
  * channels include dvres).  workspace must hold
- * psa_attention_bwd_workspace_size(shape) bytes (device, 16-byte aligned).
- * bf16 only; key_dim 32 or 64. */
+ * psa_attention_bwd_workspace_size(shape) bytes (device, 16-byte aligned); for
+ * key_dim 32 and N <= 512 one kernel computes delta on chip and leaves the
+ * workspace untouched.  bf16 only; key_dim 32 or 64. */
 psa_status_t psa_attention_bwd(const void *qkv_nchw, const void *out_nchw, const void *dout_nchw,
                                const float *lse, const void *dvres_nchw, void *dqkv_nchw,
                                void *workspace, size_t ws_bytes, psa_shape_t shape, float scale,
