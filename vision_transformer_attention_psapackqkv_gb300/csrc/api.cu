@@ -396,8 +396,8 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
   if (e != PSA_OK) return e;
   const int BH = s.B * s.num_heads;
   if (s.key_dim == 32 && s.H * s.W <= psa::kFusedBwdMaxN) {
-    // short sequences: after a delta pass, one kernel per head produces dQ, dK
-    // and dV from a single walk over its tiles
+    // short sequences: one kernel per head produces delta, dQ, dK and dV from a
+    // single walk over its tiles (the workspace is not used)
     a_dq.dvres = static_cast<const __nv_bfloat16*>(dvres);
     return from_cuda(psa::launch_psa_bwd_fused(mqk, mv, mdo, a_dq, s.key_dim, st));
   }

@@ -99,8 +99,8 @@ cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 cudaStream_t st);
 
 // Backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxN, N % 8 == 0):
-// a delta pass over Out / dOut into a.delta, then one kernel for dQ, dK and dV.
-// Same maps as launch_psa_bwd_dkdv.
+// one kernel computes delta (from a.o and a.dO, on chip; a.delta is not used), dQ,
+// dK and dV.  Same maps as launch_psa_bwd_dkdv.
 constexpr int kFusedBwdMaxN = 512;
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
                                  const CUtensorMap& mDO, const BwdArgs& a, int KD,
