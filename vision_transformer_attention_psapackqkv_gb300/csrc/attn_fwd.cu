@@ -5,8 +5,10 @@
 //
 // bf16 path (tcgen05, sm_103a): a persistent kernel.  Each CTA runs NWG
 // independent 128-query-row pipelines ("slots"); slot s of the grid takes the
-// tiles t = s, s + S, s + 2S, ... (S = slots in the grid; tile t = head t / nqt,
-// query tile t % nqt).  Warp roles:
+// tiles t = s, s + S, s + 2S, ... (S = slots in the grid).  Tiles are numbered
+// full query tiles first (t -> head t / nfull, query tile t % nfull), then the
+// partial last tile of every head (t -> head t - BH*nfull), so that the last round
+// of slots holds the cheap partial tiles.  Warp roles:
 //   warps 4w .. 4w+3   softmax of slot w: one thread per query row (= TMEM lane)
 //   warp 4*NWG         TMA producer: per slot, Q (double- or single-buffered)
 //                      and a 2- to 4-stage ring of 64-key K/V tiles
@@ -159,6 +161,18 @@ __device__ __forceinline__ float softmax_row(uint32_t (&s)[NC], int valid, float
   return alpha;
 }
 
+// Head and query tile of tile t: the BH * nfull full 128-row tiles come first,
+// then one partial tile per head (when N is not a multiple of 128).
+__device__ __forceinline__ void tile_coords(int t, int BH, int nfull, int& bh, int& qt) {
+  if (t < BH * nfull) {
+    bh = t / nfull;
+    qt = t - bh * nfull;
+  } else {
+    bh = t - BH * nfull;
+    qt = nfull;
+  }
+}
+
 // Number of tiles slot `slot` of `nslots` owns out of T.
 __device__ __forceinline__ int slot_tiles(int slot, int nslots, int T) {
   return slot < T ? (T - slot + nslots - 1) / nslots : 0;
@@ -182,6 +196,7 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
   const int N = args.N;
   const int nkv = (N + C::BN - 1) / C::BN;
   const int nqt = (N + C::BM - 1) / C::BM;
+  const int nfull = N / C::BM;  // full query tiles per head
   const int T = args.BH * nqt;
   const int nslots = gridDim.x * NWG;
 
@@ -250,7 +265,9 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
       auto issue_q = [&](int w, int i) -> bool {
         SlotBars& b = bars[w];
         const int t = blockIdx.x * NWG + w + i * nslots;
-        const int bh = t / nqt, q0 = (t % nqt) * C::BM;
+        int bh, qt;
+        tile_coords(t, args.BH, nfull, bh, qt);
+        const int q0 = qt * C::BM;
         const int qb = i % QBUF;
         if (i >= QBUF && !mbar_wait(&b.q_empty[qb], ((i / QBUF) - 1) & 1, abort)) return false;
         mbar_arrive_expect_tx(&b.q_full[qb], C::Q_BYTES);
@@ -274,7 +291,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
             if (i >= ntiles[w]) continue;
             SlotBars& b = bars[w];
             const int t = blockIdx.x * NWG + w + i * nslots;
-            const int bh = t / nqt;
+            int bh, qt_unused;
+            tile_coords(t, args.BH, nfull, bh, qt_unused);
             const int g = i * nkv + j, st = g % C::STAGES;
             if (g >= C::STAGES && !mbar_wait(&b.kv_empty[st], ((g / C::STAGES) - 1) & 1, abort)) {
               ok = false;
@@ -402,7 +420,9 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
     bool ok = true;
     for (int i = 0; ok && i < my_tiles; ++i) {
       const int t = blockIdx.x * NWG + w + i * nslots;
-      const int bh = t / nqt, qt = t % nqt, q0 = qt * C::BM;
+      int bh, qt;
+      tile_coords(t, args.BH, nfull, bh, qt);
+      const int q0 = qt * C::BM;
       const bool active = wq * 32 < N - q0;  // the warp has live rows
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkv; ++j) {
