@@ -46,11 +46,13 @@ def errors(x: np.ndarray, ref: np.ndarray):
 
 
 def assert_close(x: np.ndarray, ref: np.ndarray, dtype: str, what: str = "",
-                 output_rounding: bool = False):
+                 output_rounding: bool = False, roundings: int = 1):
     """The bars above.  With output_rounding, each bf16 element may in addition be
     off by half a bf16 ulp of its reference (2^-8 |ref|): used where the outputs
     reach magnitudes >= 4 (a residual gradient added into dV), at which rounding
-    to bf16 alone can move a value by more than 1.5e-2."""
+    to bf16 alone can move a value by more than 1.5e-2.  roundings = 2 is for a sum
+    of two results that were each rounded to bf16 before the sum (the two-call
+    chain's dQ and dK): its mean-relative bar is twice the single-rounding one."""
     assert x.shape == ref.shape, (what, x.shape, ref.shape)
     assert np.all(np.isfinite(x)), f"{what}: non-finite values"
     max_abs, mean_rel = errors(x, ref)
@@ -62,5 +64,6 @@ def assert_close(x: np.ndarray, ref: np.ndarray, dtype: str, what: str = "",
             assert excess <= 0, f"{what}: error exceeds 1.5e-2 + 2^-8|ref| by {excess:.3e}"
         else:
             assert max_abs <= BF16_MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {BF16_MAX_ABS}"
-        assert mean_rel <= BF16_MEAN_REL, f"{what}: mean-rel {mean_rel:.3e} > {BF16_MEAN_REL}"
+        bar = BF16_MEAN_REL * roundings
+        assert mean_rel <= bar, f"{what}: mean-rel {mean_rel:.3e} > {bar}"
     return max_abs, mean_rel
