@@ -10,9 +10,10 @@
 // partial last tile of every head (t -> head t - BH*nfull), so that the last round
 // of slots holds the cheap partial tiles.  Warp roles:
 //   warps 4w .. 4w+3   softmax of slot w: one thread per query row (= TMEM lane)
-//   warp 4*NWG         TMA producer: per slot, Q (double- or single-buffered)
+//                      (split rows: warps 0-7 of the single slot, see below)
+//   next warp (P)      TMA producer: per slot, Q (double- or single-buffered)
 //                      and a 2- to 4-stage ring of 64-key K/V tiles
-//   warp 4*NWG + 1     MMA issuer (one thread) and TMEM owner; per slot
+//   warp P + 1         MMA issuer (one thread) and TMEM owner; per slot
 //                        S_k = Q K_k^T -> TMEM (64 columns)
 //                        O  += P_k V_k -> TMEM (DV columns), P_k from shared
 //                        memory (double-buffered)
@@ -24,6 +25,9 @@
 // each thread owning one 32-key half of every tile with its own running max and
 // sum and its own O accumulator in TMEM (P.V k-steps of half h go to accumulator
 // h); the epilogue merges the halves, O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l.
+// Every CTA sets up its barriers and TMEM, lets the next kernel of the stream
+// start (programmatic dependent launch) and waits for the previous one before
+// touching global memory.
 // Softmax: running max in the log2 domain; p = 2^(scale*log2e*s - m) rounded to
 // bf16 into P (K-major, 128-byte swizzle); O is rescaled in TMEM only when a row
 // max grows by more than 2^8 (exact either way, since O and the running sum
