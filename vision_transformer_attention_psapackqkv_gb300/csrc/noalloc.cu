@@ -57,8 +57,10 @@ extern "C" psa_status_t psa_attention_bwd_noalloc(const void* qkv_nchw, const vo
   void* scratch = nullptr;
   psa_status_t e = delta_scratch(&scratch);
   if (e != PSA_OK) return e;
-  // The delta values are fully written by the dQ kernel before the dK/dV kernel
-  // reads them, so nothing left in the array by an earlier call needs clearing.
+  // Where the two-kernel backward runs, the dQ kernel writes every delta value
+  // before the dK/dV kernel reads it, so nothing left in the array by an earlier
+  // call needs clearing; the one-kernel backward (key_dim 32, N <= 512) keeps
+  // delta on chip and does not touch the array.
   return psa_attention_bwd(qkv_nchw, out_nchw, dout_nchw, lse, dvres_nchw, dqkv_nchw, scratch,
                            kMaxDeltaFloats * sizeof(float), shape, scale, stream);
 }
