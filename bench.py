@@ -15,6 +15,10 @@ FlashAttention-2 calls over BH=64, N in {1024, 4096, 16384}, d in {32, 64}
 (forward, and dQ + dK/dV backward) and the N=1600 PSA step (B=32, 8 heads,
 40x40), as TFLOP/s and as a fraction of the bf16 tensor peak.
 
+--layout times the data-movement kernels instead (pack, its inverse, merge, its
+inverse, extract) as GB/s against the measured HBM bandwidth, cold and hot L2,
+and the unfused pack -> FA2 x 2 -> merge chain next to the fused calls.
+
 --impl reference times the fp64 CPU oracle (the test oracle, untuned) on the
 host cores, on a bounded sample of the same workload per step.
 
@@ -578,6 +582,122 @@ def run_sweep(args):
     return lines
 
 
+def run_layout(args):
+    """The data-movement kernels (PsaPackQkv, its inverse, PsaMergeAttn, its inverse,
+    PsaExtractV) on the psa_fwdbwd_n400 workload, as GB/s of algorithmic bytes
+    (every element read once and written once) against the measured HBM copy
+    bandwidth, with L2 cold (enough buffer sets rotate to exceed twice the L2) and
+    hot (one set, which fits in L2).  Then the unfused chain the pages describe
+    (PsaPackQkv -> Flash Attention 2 on V_lo and on V_hi -> PsaMergeAttn, and
+    PsaExtractV) next to the fused psa_attention_fwd, and the unfused backward
+    (inverse merge -> dQ and dK/dV kernels per V half -> inverse pack; the sum of
+    the two halves' dQ and dK has no kernel of its own and is left out) next to
+    psa_attention_bwd.  One JSON line per case."""
+    import torch
+
+    from vision_transformer_attention_psapackqkv_gb300 import binding as B
+    from vision_transformer_attention_psapackqkv_gb300.inputs import PSA_WORKLOADS
+
+    peaks, src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    w = PSA_WORKLOADS[WORKLOAD]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed)
+    rnd = lambda *shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    BH, N, KD = w.BH, w.N, w.key_dim
+    scale = 1.0 / math.sqrt(KD)
+
+    def make_set():
+        qkv = rnd(w.B, w.qkv_channels, w.H, w.W)
+        dout = rnd(w.B, w.out_channels, w.H, w.W)
+        st = {"qkv": qkv, "dout": dout, "packed": torch.empty((4, BH, N, KD), dtype=torch.bfloat16, device="cuda"),
+              "out": torch.empty_like(dout), "v": torch.empty_like(dout), "dqkv": torch.empty_like(qkv),
+              "lse": torch.empty((BH, N), dtype=torch.float32, device="cuda"),
+              "lse2": torch.empty((BH, N), dtype=torch.float32, device="cuda"),
+              "delta": torch.empty((BH, N), dtype=torch.float32, device="cuda")}
+        st["o"] = torch.empty((2, BH, N, KD), dtype=torch.bfloat16, device="cuda")
+        st["do"] = torch.empty((2, BH, N, KD), dtype=torch.bfloat16, device="cuda")
+        st["dpacked"] = torch.empty((4, BH, N, KD), dtype=torch.bfloat16, device="cuda")
+        st["dqk_hi"] = torch.empty((2, BH, N, KD), dtype=torch.bfloat16, device="cuda")
+        st["ws"] = torch.empty(B.psa_attention_bwd_workspace_size(B.shape_of(qkv, w.num_heads, KD)),
+                               dtype=torch.uint8, device="cuda")
+        return st
+
+    per_set = sum(t.numel() * t.element_size() for t in make_set().values())
+    nsets = max(3, math.ceil(2 * 2 * 129e6 / per_set))
+    sets = [make_set() for _ in range(nsets)]
+    shape = B.shape_of(sets[0]["qkv"], w.num_heads, KD)
+    e = 2
+    qkv_b, half_b = w.B * w.qkv_channels * N * e, w.B * w.out_channels * N * e
+    cases = [
+        ("psa_pack_qkv", 2 * qkv_b, lambda s: B.psa_pack_qkv(s["qkv"], s["packed"], shape)),
+        ("psa_unpack_qkv", 2 * qkv_b, lambda s: B.psa_unpack_qkv(s["packed"], s["dqkv"], shape)),
+        ("psa_merge_attn", 2 * half_b, lambda s: B.psa_merge_attn(s["o"][0], s["o"][1], s["out"], shape)),
+        ("psa_unmerge_attn", 2 * half_b, lambda s: B.psa_unmerge_attn(s["dout"], s["do"][0], s["do"][1], shape)),
+        ("psa_extract_v", 2 * half_b, lambda s: B.psa_extract_v(s["qkv"], s["v"], shape)),
+    ]
+    lines = []
+    iters = 200
+    for name, nbytes, fn in cases:
+        for l2 in ("cold", "hot"):
+            use = sets if l2 == "cold" else sets[:1]
+            with ClockSampler() as clk:
+                sec = _time_loop(torch, lambda i: fn(use[i % len(use)]), iters, 2 * len(use))
+            gbs = nbytes / sec / 1e9
+            line = {"metric": "layout kernel GB/s (algorithmic bytes)", "workload": WORKLOAD,
+                    "kernel": name, "l2": l2, "value": gbs, "unit": "GB/s", "us": sec * 1e6,
+                    "bytes": nbytes, "hbm": {"peak": hbm, "frac": gbs / hbm, "peak_source": src},
+                    "clocks": clk.summary()}
+            lines.append(line)
+            print(json.dumps(line), flush=True)
+
+    def fwd_chain(s):
+        B.psa_pack_qkv(s["qkv"], s["packed"], shape)
+        q, k, vlo, vhi = s["packed"]
+        B.flash_attn2_fwd(q, k, vlo, s["o"][0], s["lse"], scale)
+        B.flash_attn2_fwd(q, k, vhi, s["o"][1], s["lse2"], scale)
+        B.psa_merge_attn(s["o"][0], s["o"][1], s["out"], shape)
+        B.psa_extract_v(s["qkv"], s["v"], shape)
+
+    def fwd_fused(s):
+        B.psa_attention_fwd(s["qkv"], s["out"], s["lse"], s["v"], shape, scale)
+
+    def bwd_chain(s):
+        q, k, vlo, vhi = s["packed"]
+        B.psa_unmerge_attn(s["dout"], s["do"][0], s["do"][1], shape)
+        dq, dk, dvlo, dvhi = s["dpacked"]
+        B.flash_attn2_bwd_dq(q, k, vlo, s["o"][0], s["do"][0], s["lse"], s["delta"], dq, scale)
+        B.flash_attn2_bwd_dkdv(q, k, vlo, s["do"][0], s["lse"], s["delta"], dk, dvlo, scale)
+        B.flash_attn2_bwd_dq(q, k, vhi, s["o"][1], s["do"][1], s["lse"], s["delta"], s["dqk_hi"][0], scale)
+        B.flash_attn2_bwd_dkdv(q, k, vhi, s["do"][1], s["lse"], s["delta"], s["dqk_hi"][1], dvhi, scale)
+        B.psa_unpack_qkv(s["dpacked"], s["dqkv"], shape)
+
+    def bwd_fused(s):
+        B.psa_attention_bwd(s["qkv"], s["out"], s["dout"], s["lse"], None, s["dqkv"], s["ws"], shape, scale)
+
+    for st in sets:
+        fwd_chain(st)
+    kmodel, _ = work_model(w)
+    for name, fn, nk, part in (("unfused forward chain", fwd_chain, 5, "fwd"),
+                               ("psa_attention_fwd", fwd_fused, 1, "fwd"),
+                               ("unfused backward chain (without the dQ / dK half sums)", bwd_chain, 6, "bwd"),
+                               ("psa_attention_bwd", bwd_fused, 1, "bwd")):
+        with ClockSampler() as clk:
+            sec = _time_loop(torch, lambda i: fn(sets[i % nsets]), iters, 2 * nsets)
+        km = kmodel[part]
+        line = {"metric": "PSA attention step part, unfused chain vs fused", "workload": WORKLOAD,
+                "path": name, "launches": nk, "us": sec * 1e6, "l2": "cold",
+                "tflops": km["flops"] / sec / 1e12,
+                "hbm": {"algorithmic_bytes": km["bytes"], "gbs": km["bytes"] / sec / 1e9,
+                        "frac": km["bytes"] / sec / 1e9 / hbm, "peak_source": src},
+                "clocks": clk.summary()}
+        lines.append(line)
+        print(json.dumps(line), flush=True)
+    if B.psa_get_last_device_error() != 0:
+        raise RuntimeError("device error in the layout bench")
+    return lines
+
+
 def run_reference(args):
     from vision_transformer_attention_psapackqkv_gb300.inputs import PSA_WORKLOADS
 
@@ -627,6 +747,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--split-bwd", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--layout", action="store_true",
+                    help="time the data-movement kernels and the unfused chain instead")
     ap.add_argument("--case", default=None,
                     help="with --sweep: run only the case of this name (e.g. fa2_bh64_n4096_d64)")
     args = ap.parse_args()
@@ -642,6 +764,10 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.layout:
+        if rank == 0:
+            run_layout(args)
         return
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:

@@ -163,16 +163,21 @@ psa_status_t psa_attention_bwd_dkdv(const void *qkv_nchw, const void *dout_nchw,
  * the backward (for example a plugin whose host framework owns all device
  * allocations, or a latency-critical loop where cudaMalloc / cudaFree would
  * synchronise the device).  The pages have no counterpart: this is a
- * convenience of this library.  Same arguments, results and errors as
+ * convenience of this library.  Same arguments and results as
  * psa_attention_bwd, minus the workspace.  The delta scratch lives in a fixed
  * 4 MiB array inside the library's device memory, which every GPU that loads the
  * library keeps until the process exits; B * num_heads * H * W may not exceed
- * 1048576 (PSA_ERR_UNSUPPORTED otherwise).  The first call on each device, made
- * with that device current, looks up the array's address; make that first call
- * before any stream capture.  All calls share the one array: calls whose kernels
- * overlap on the GPU (other streams, other threads) race on it, so serialise
- * them.  Nothing in the array needs clearing between calls.  No allocation of
- * any kind is made. */
+ * 1048576.  Errors are checked in this order: a NULL required pointer or an
+ * invalid shape (PSA_ERR_INVALID_ARG), then that limit (PSA_ERR_UNSUPPORTED),
+ * then every other check of psa_attention_bwd.  The first call on each device,
+ * made with that device current, looks up the array's address; make that first
+ * call before any stream capture.  Only the two-kernel form of the backward
+ * (key_dim 64, or N > 512) uses the array; the one-kernel form (key_dim 32,
+ * N <= 512) keeps delta on chip.  All calls of the two-kernel form share the one
+ * array: such calls whose kernels overlap on the GPU (other streams, other
+ * threads) race on it, so serialise them.  Nothing in the array needs clearing
+ * between calls (each call writes every value it reads).  No allocation of any
+ * kind is made. */
 psa_status_t psa_attention_bwd_noalloc(const void *qkv_nchw, const void *out_nchw,
                                        const void *dout_nchw, const float *lse,
                                        const void *dvres_nchw, void *dqkv_nchw, psa_shape_t shape,
@@ -189,6 +194,14 @@ const char *psa_status_string(psa_status_t status);
 /* Synchronises the stream, then reads and clears the device-side error word
  * (PSA_ERR_TIMEOUT after a bounded on-chip wait gave up; PSA_OK otherwise). */
 psa_status_t psa_get_last_device_error(cudaStream_t stream);
+
+/* Diagnostic of the failure path (no counterpart on the pages): launches one warp
+ * that waits, through the same bounded on-chip wait as the attention kernels but
+ * with a limit of limit_ns nanoseconds (1 .. 100,000,000), on a barrier that
+ * nothing arrives at.  The wait gives up, records PSA_ERR_TIMEOUT in the device
+ * error word (read it with psa_get_last_device_error) and the kernel returns; the
+ * context stays usable.  PSA_ERR_INVALID_ARG for a limit outside that range. */
+psa_status_t psa_debug_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

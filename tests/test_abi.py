@@ -134,3 +134,9 @@ def test_fused_validation(lib):
     assert d(A, A, A, A, MIS, A, _shape(), 0.17, None) == ALIGNMENT
     assert k(A, A, A, None, None, A, _shape(), 0.17, None) == INVALID              # delta required
     assert k(A, A, A, A, MIS, A, _shape(), 0.17, None) == ALIGNMENT
+
+
+def test_debug_wait_limit_validation(lib):
+    # rejected before any launch: the limit must lie in 1 ns .. 100 ms
+    assert lib.psa_debug_wait_timeout(0, None) == INVALID
+    assert lib.psa_debug_wait_timeout(100_000_001, None) == INVALID

@@ -18,6 +18,11 @@ SHAPES = [
     (2, 3, 8, 5, 7, "bf16"),       # ragged: N = 35, tiles of 64 leave a tail
     (3, 1, 64, 1, 1, "f32"),       # a single position
     (1, 2, 16, 9, 15, "f32"),      # N = 135
+    # 16-byte vector path (bf16, N % 8 == 0, KD % 8 == 0): tiles of 512 positions
+    (1, 2, 64, 12, 12, "bf16"),    # key_dim 64, one partial tile
+    (1, 1, 128, 16, 40, "bf16"),   # key_dim 128, N = 640: a full tile and a partial one
+    (2, 3, 8, 4, 6, "bf16"),       # key_dim 8, N = 24
+    (1, 1, 16, 8, 129, "bf16"),    # N = 1032: two full tiles and one chunk of 8
 ]
 
 

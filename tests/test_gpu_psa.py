@@ -192,6 +192,16 @@ def test_unfused_chain_matches_oracle_and_fused(oracle, Bn, nh, KD, H, W):
         B.flash_attn2_bwd_dq(q, k, v_h, o_h, do_h, lse, delta, dq, scale)
         B.flash_attn2_bwd_dkdv(q, k, v_h, do_h, lse, delta, dk, dv, scale)
         grads.append((dq, dk, dv))
+    torch.cuda.synchronize()
+    # each FA2 backward call on its own, at the single-rounding bars: the oracle's
+    # attention backward of that V half
+    p64 = storage_to_f64(oracle.pack_qkv(ins["qkv"], nh, KD), "bf16")
+    do64 = [storage_to_f64(x, "bf16") for x in oracle.unmerge_attn(ins["dout"], nh, KD)]
+    for half, (dq, dk, dv) in enumerate(grads):
+        rq, rk, rv = oracle.attn_bwd(p64[0], p64[1], p64[2 + half], do64[half], scale)
+        assert_close(to_host_f64(dq), rq, "bf16", f"half {half} dQ")
+        assert_close(to_host_f64(dk), rk, "bf16", f"half {half} dK")
+        assert_close(to_host_f64(dv), rv, "bf16", f"half {half} dV")
     dpacked = torch.stack([(grads[0][0].float() + grads[1][0].float()).to(torch.bfloat16),
                            (grads[0][1].float() + grads[1][1].float()).to(torch.bfloat16),
                            grads[0][2], grads[1][2]]).contiguous()
@@ -200,7 +210,9 @@ def test_unfused_chain_matches_oracle_and_fused(oracle, Bn, nh, KD, H, W):
     ref_dqkv = oracle.psa_bwd(q64, storage_to_f64(ins["dout"], "bf16"), nh, KD, scale)
     got = to_host_f64(dqkv).reshape(Bn, nh, 4, KD, -1)
     ref = ref_dqkv.reshape(Bn, nh, 4, KD, -1)
-    # dQ and dK are sums of the two halves' bf16 outputs (two roundings); dV halves one
+    # end to end through the chain: dQ and dK are sums of the two halves' bf16
+    # outputs (two roundings, checked per half above at the single-rounding bars);
+    # the dV halves carry one
     for s, name in enumerate(("dQ", "dK", "dV_lo", "dV_hi")):
         assert_close(got[:, :, s], ref[:, :, s], "bf16", "chain " + name, roundings=2 if s < 2 else 1)
 

@@ -36,7 +36,7 @@ EXPORTED = (
     "flash_attn2_fwd", "flash_attn2_bwd_dq", "flash_attn2_bwd_dkdv", "psa_attention_fwd",
     "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv", "psa_attention_bwd_noalloc",
     "psa_attention_bwd_workspace_size", "psa_status_string",
-    "psa_get_last_device_error",
+    "psa_get_last_device_error", "psa_debug_wait_timeout",
 )
 
 
@@ -71,6 +71,7 @@ def load(path: str | None = None):
         "psa_attention_bwd_workspace_size": [S],
         "psa_status_string": [I],
         "psa_get_last_device_error": [P],
+        "psa_debug_wait_timeout": [ctypes.c_ulonglong, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -198,6 +199,10 @@ def psa_attention_bwd_noalloc(qkv, out, dout, lse, dvres, dqkv, shape: PsaShape,
 
 def psa_get_last_device_error(stream=None) -> int:
     return int(load().psa_get_last_device_error(_stream(stream)))
+
+
+def psa_debug_wait_timeout(limit_ns: int, stream=None):
+    _check("psa_debug_wait_timeout", load().psa_debug_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def psa_status_string(status: int) -> str:

@@ -7,13 +7,64 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "../../include/psa.h"
 #include "attn.cuh"
+#include "ptx.cuh"
 #include "layout.cuh"
 
 namespace psa {
 __device__ int g_device_error = 0;
+
+namespace {
+// One CTA of one warp waits, through the same bounded wait as the attention
+// kernels, on an mbarrier that nothing ever arrives at, so the wait gives up
+// after limit_ns, records PSA_ERR_TIMEOUT in g_device_error and the kernel
+// returns.  Nothing is left waiting and no global memory besides the error word
+// is touched.
+__global__ void __launch_bounds__(32) wait_timeout_probe_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait(&bar, 0, &abort, limit_ns);
 }
+}  // namespace
+
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+cudaError_t set_max_dynamic_smem(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;  // (kernel, device)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kern, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kern, dev});
+  return e;
+}
+}  // namespace psa
 
 namespace {
 
@@ -114,6 +165,12 @@ const char* psa_status_string(psa_status_t s) {
     case PSA_ERR_TIMEOUT: return "PSA_ERR_TIMEOUT: an on-chip wait gave up";
   }
   return "unknown psa_status_t";
+}
+
+psa_status_t psa_debug_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 100000000ull) return PSA_ERR_INVALID_ARG;
+  psa::wait_timeout_probe_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_ns);
+  return from_cuda(cudaGetLastError());
 }
 
 psa_status_t psa_get_last_device_error(cudaStream_t stream) {

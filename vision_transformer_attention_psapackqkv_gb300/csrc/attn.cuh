@@ -32,7 +32,6 @@ cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, f
 cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, int nh, int KD,
                                int N, float scale, cudaStream_t st);
 
-// Multiprocessor count of the current device (queried once; persistent grids).
 // Launches kern with programmatic stream serialization: its CTAs may become
 // resident and run their prologue (barrier set-up, tensor memory allocation)
 // while the previous kernel of the stream finishes; the kernels call pdl_wait()
@@ -53,16 +52,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
-inline int device_sm_count() {
-  static const int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
-    return v;
-  }();
-  return n;
-}
+// Multiprocessor count of the current device, queried once per device (devices of
+// one process may differ, e.g. a partitioned GPU next to a whole one).
+int device_sm_count();
+
+// Raises the dynamic shared memory limit of kernel `kern` to `bytes` on the
+// current device (a per-device attribute), once per kernel and device.
+cudaError_t set_max_dynamic_smem(const void* kern, int bytes);
 
 struct BwdArgs {
   int N;

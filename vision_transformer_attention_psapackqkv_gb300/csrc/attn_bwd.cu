@@ -731,8 +731,7 @@ __global__ void __launch_bounds__(192, CPS)
 template <typename Cfg, int CPS, typename K, typename... Maps>
 cudaError_t launch(K kern, const BwdArgs& a, int rows_per_unit, cudaStream_t st,
                    const Maps&... maps) {
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  const cudaError_t attr = set_max_dynamic_smem((const void*)kern, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   const long long units = (long long)a.BH * ((a.N + rows_per_unit - 1) / rows_per_unit);
   const long long ctas = std::min<long long>((long long)CPS * device_sm_count(), units);

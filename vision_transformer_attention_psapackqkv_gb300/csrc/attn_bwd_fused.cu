@@ -558,8 +558,7 @@ cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
     return cudaErrorInvalidValue;
   using Cfg = FusedCfg<32, 64, 4>;
   auto kern = attn_bwd_fused_kernel<32, 64, 4>;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  const cudaError_t attr = set_max_dynamic_smem((const void*)kern, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   const int ctas = std::min(device_sm_count(), a.BH);
   return launch_pdl(kern, dim3(ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st, mQK, mQK, mV,

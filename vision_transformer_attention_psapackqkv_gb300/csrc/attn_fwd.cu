@@ -691,29 +691,18 @@ __global__ void __launch_bounds__(128)
 }
 
 
-int sm_count() {
-  static const int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
-    return v;
-  }();
-  return n;
-}
 
 template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
 cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUtensorMap& mV,
                       const FwdArgs& a, cudaStream_t st) {
   using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  const cudaError_t attr = set_max_dynamic_smem((const void*)kern, C::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   // persistent grid: one CTA per SM with two slots, or two single-slot CTAs per SM
   const long long T = (long long)a.BH * ((a.N + C::BM - 1) / C::BM);
   const long long per_sm = NWG == 1 ? 2 : 1;
-  const long long ctas = std::min<long long>(per_sm * sm_count(), (T + NWG - 1) / NWG);
+  const long long ctas = std::min<long long>(per_sm * device_sm_count(), (T + NWG - 1) / NWG);
   return launch_pdl(kern, dim3((unsigned)ctas), dim3(C::kThreads), C::SMEM_BYTES, st, mQK, mK,
                     mV, a);
 }

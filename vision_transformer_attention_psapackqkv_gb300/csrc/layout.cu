@@ -7,11 +7,15 @@
 //   channels_to_rows: a block of KD channels x N positions (NCHW, positions
 //     contiguous) -> N rows x KD (row-major, KD contiguous).   pack, unmerge
 //   rows_to_channels: the inverse direction.                   unpack, merge
-// Each CTA moves a tile of KD channels x 64 positions through shared memory so
-// that both the global loads and the global stores are coalesced.  ExtractV is
-// a strided copy of contiguous per-head slabs in 16-byte vectors.
+// Each CTA moves a tile of channels x positions through shared memory so that
+// both the global loads and the global stores are coalesced: for bf16 with
+// 16-byte aligned rows (N % 8 == 0, KD % 8 == 0, every shape the fused kernels
+// take) in 16-byte vectors on both sides; otherwise (fp32, or rows that are not
+// 16-byte multiples) one element per thread.  ExtractV is a strided copy of
+// contiguous per-head slabs in 16-byte vectors.
 #include <stdint.h>
 
+#include "attn.cuh"
 #include "layout.cuh"
 
 namespace psa {
@@ -85,6 +89,132 @@ __global__ void __launch_bounds__(kThreads) rows_to_channels_kernel(TransposeArg
   }
 }
 
+// ---------------------------------------------------------------- 16-byte vectors
+// The same two transposes for bf16 when every channel row and every position row
+// starts on a 16-byte boundary (N % 8 == 0 and KD % 8 == 0): each CTA moves a tile
+// of KD channels x up to 512 positions of one (batch, head, plane); global memory
+// is read and written only in 16-byte vectors (8 elements), four per thread in
+// flight at a time, and shared memory holds the tile as 16-byte chunks (chunk
+// (d, c) = channel d, positions 8c .. 8c+7), row-major with the chunk index XOR-ed
+// with (d / 8) % 8.  The element-wise side of the transpose (8 channels of one
+// position per thread) then reads 8 different chunks per instruction across a warp
+// without bank conflicts, and the chunk-wise side stays conflict-free.
+constexpr int kVecTileN = 512;
+constexpr int kVecChunks = kVecTileN / 8;  // 16-byte chunks per channel row of the tile
+
+__device__ __forceinline__ int vec_chunk(int d, int c) { return d * kVecChunks + (c ^ ((d >> 3) & 7)); }
+
+// Plane pointer s of four without a local-memory copy of the array.
+template <typename P>
+__device__ __forceinline__ P plane_ptr(const P (&p)[4], int s) {
+  return s == 0 ? p[0] : s == 1 ? p[1] : s == 2 ? p[2] : p[3];
+}
+
+__global__ void __launch_bounds__(kThreads) channels_to_rows_vec_kernel(const TransposeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint4* tile = reinterpret_cast<uint4*>(smem_raw);  // KD x kVecChunks chunks
+  const uint16_t* tile16 = reinterpret_cast<const uint16_t*>(smem_raw);
+  const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
+  const int unit = blockIdx.x / ntiles;
+  const int s = unit % a.planes;
+  const int bhd = unit / a.planes;  // b * nh + head
+  const int head = bhd % a.nh, b = bhd / a.nh;
+  const int n0 = (blockIdx.x % ntiles) * kVecTileN;
+  const int nvalid = min(kVecTileN, a.N - n0);
+  const int cvalid = nvalid / 8;  // N % 8 == 0, so the tile holds whole chunks
+  const uint16_t* src = static_cast<const uint16_t*>(a.nchw_src) +
+                        ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
+                         (long long)s * a.KD) * a.N + n0;
+  const int nload = a.KD * cvalid;
+  for (int i0 = threadIdx.x; i0 < nload; i0 += 4 * kThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = i0 + u * kThreads;
+      if (idx < nload) {
+        const int d = idx / cvalid, c = idx - d * cvalid;
+        v[u] = __ldg(reinterpret_cast<const uint4*>(src + (long long)d * a.N + 8 * c));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = i0 + u * kThreads;
+      if (idx < nload) {
+        const int d = idx / cvalid, c = idx - d * cvalid;
+        tile[vec_chunk(d, c)] = v[u];
+      }
+    }
+  }
+  __syncthreads();
+  const int dvec = a.KD / 8;
+  uint4* dst = reinterpret_cast<uint4*>(plane_ptr(a.rows_dst, s)) +
+               ((long long)bhd * a.N + n0) * dvec;
+  const int nstore = nvalid * dvec;
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < nstore; idx += kThreads) {
+    const int n = idx / dvec, g = idx - n * dvec;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int d0 = 8 * g + 2 * e;
+      const uint32_t lo = tile16[vec_chunk(d0, n >> 3) * 8 + (n & 7)];
+      const uint32_t hi = tile16[vec_chunk(d0 + 1, n >> 3) * 8 + (n & 7)];
+      w[e] = lo | (hi << 16);
+    }
+    dst[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) rows_to_channels_vec_kernel(const TransposeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint4* tile = reinterpret_cast<const uint4*>(smem_raw);
+  uint16_t* tile16 = reinterpret_cast<uint16_t*>(smem_raw);
+  const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
+  const int unit = blockIdx.x / ntiles;
+  const int s = unit % a.planes;
+  const int bhd = unit / a.planes;
+  const int head = bhd % a.nh, b = bhd / a.nh;
+  const int n0 = (blockIdx.x % ntiles) * kVecTileN;
+  const int nvalid = min(kVecTileN, a.N - n0);
+  const int cvalid = nvalid / 8;
+  const int dvec = a.KD / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(plane_ptr(a.rows_src, s)) +
+                     ((long long)bhd * a.N + n0) * dvec;
+  const int nload = nvalid * dvec;
+  for (int i0 = threadIdx.x; i0 < nload; i0 += 4 * kThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = i0 + u * kThreads;
+      if (idx < nload) v[u] = __ldg(src + idx);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = i0 + u * kThreads;
+      if (idx < nload) {
+        const int n = idx / dvec, g = idx - n * dvec;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d0 = 8 * g + 2 * e;
+          tile16[vec_chunk(d0, n >> 3) * 8 + (n & 7)] = (uint16_t)(w[e] & 0xffffu);
+          tile16[vec_chunk(d0 + 1, n >> 3) * 8 + (n & 7)] = (uint16_t)(w[e] >> 16);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  uint16_t* dst = static_cast<uint16_t*>(a.nchw_dst) +
+                  ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
+                   (long long)s * a.KD) * a.N + n0;
+  const int nstore = a.KD * cvalid;
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < nstore; idx += kThreads) {
+    const int d = idx / cvalid, c = idx - d * cvalid;
+    *reinterpret_cast<uint4*>(dst + (long long)d * a.N + 8 * c) = tile[vec_chunk(d, c)];
+  }
+}
+
 // Copies `slabs` contiguous slabs of slab_vec 16-byte vectors from src (slab
 // stride src_stride_vec) to dst (slab stride dst_stride_vec).
 __global__ void __launch_bounds__(kThreads)
@@ -116,6 +246,22 @@ cudaError_t launch_transpose(bool to_rows, const TransposeArgs& a, int B, cudaSt
 
 cudaError_t transpose(bool to_rows, const TransposeArgs& a, int B, int elem_bytes,
                       cudaStream_t st) {
+  if (elem_bytes == 2 && a.N % 8 == 0 && a.KD % 8 == 0) {
+    // bf16 with 16-byte aligned channel and position rows: 16-byte vectors
+    const long long tiles =
+        (long long)((a.N + kVecTileN - 1) / kVecTileN) * B * a.nh * a.planes;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)a.KD * kVecTileN * 2;  // up to 128 KB (KD = 128)
+    const cudaError_t attr = set_max_dynamic_smem(
+        to_rows ? (const void*)channels_to_rows_vec_kernel : (const void*)rows_to_channels_vec_kernel,
+        128 * kVecTileN * 2);  // the largest tile (key_dim 128), set once per device
+    if (attr != cudaSuccess) return attr;
+    if (to_rows)
+      channels_to_rows_vec_kernel<<<(unsigned)tiles, kThreads, smem, st>>>(a);
+    else
+      rows_to_channels_vec_kernel<<<(unsigned)tiles, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+  }
   return elem_bytes == 2 ? launch_transpose<uint16_t>(to_rows, a, B, st)
                          : launch_transpose<uint32_t>(to_rows, a, B, st);
 }

@@ -50,6 +50,9 @@ extern "C" psa_status_t psa_attention_bwd_noalloc(const void* qkv_nchw, const vo
                                                   const void* dvres_nchw, void* dqkv_nchw,
                                                   psa_shape_t shape, float scale,
                                                   cudaStream_t stream) {
+  // the checks psa_attention_bwd makes first (required pointers, the shape), then
+  // the capacity of the array, then everything else psa_attention_bwd checks
+  if (!qkv_nchw || !out_nchw || !dout_nchw || !lse || !dqkv_nchw) return PSA_ERR_INVALID_ARG;
   const size_t ws = psa_attention_bwd_workspace_size(shape);
   if (ws == 0) return PSA_ERR_INVALID_ARG;
   if ((size_t)shape.B * shape.num_heads * shape.H * shape.W > kMaxDeltaFloats)
@@ -57,10 +60,11 @@ extern "C" psa_status_t psa_attention_bwd_noalloc(const void* qkv_nchw, const vo
   void* scratch = nullptr;
   psa_status_t e = delta_scratch(&scratch);
   if (e != PSA_OK) return e;
-  // Where the two-kernel backward runs, the dQ kernel writes every delta value
-  // before the dK/dV kernel reads it, so nothing left in the array by an earlier
-  // call needs clearing; the one-kernel backward (key_dim 32, N <= 512) keeps
-  // delta on chip and does not touch the array.
+  // Where the two-kernel backward runs (key_dim 64, or N > 512), the dQ kernel
+  // writes every delta value of this call before the dK/dV kernel reads it, so
+  // nothing an earlier call left in the array needs clearing; the one-kernel
+  // backward (key_dim 32, N <= 512) keeps delta on chip and does not touch the
+  // array, so only two-kernel calls can race on it.
   return psa_attention_bwd(qkv_nchw, out_nchw, dout_nchw, lse, dvres_nchw, dqkv_nchw, scratch,
                            kMaxDeltaFloats * sizeof(float), shape, scale, stream);
 }

@@ -70,16 +70,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Waits for the phase of `parity` to complete.  Gives up (returns false) when
-// another warp of the CTA raised *abort, or after kWaitLimitNs, in which case it
-// raises *abort and records PSA_ERR_TIMEOUT in the device error word.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// another warp of the CTA raised *abort, or after limit_ns (kWaitLimitNs in every
+// attention kernel), in which case it raises *abort and records PSA_ERR_TIMEOUT
+// in the device error word.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
   const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       atomicExch(&g_device_error, 5);
       return false;

@@ -131,3 +131,68 @@ def fa2_inputs(BH: int, N: int, d: int, dtype: str, seed: int, value_scale: floa
     """Q, K, V, dO of shape [BH, N, d] in storage form."""
     return {name: to_storage(normal_f32((BH, N, d), seed, value_scale, i), dtype)
             for i, name in enumerate(("q", "k", "v", "do"))}
+
+
+# --------------------------------------------------------------------------- planted score growth
+def planted_direction(d: int, seed: int) -> np.ndarray:
+    """A seeded unit vector of length d (float32)."""
+    u = normal_f32((d,), seed, 1.0, 7).astype(np.float64)
+    return (u / np.linalg.norm(u)).astype(np.float32)
+
+
+def planted_shifts(N: int, d: int, scale: float, seed: int, mode: str, tile: int = 64,
+                   growth_log2: float = 10.0, q_shift: float = 3.0):
+    """Additive offsets (float32) for query and key rows of one head that make the
+    scores of a query row grow along the key sequence, so that an online softmax
+    over key tiles meets a row maximum that rises by more than 2^8 after its first
+    tile (the case in which a lazily rescaled accumulator must be rescaled).
+
+    Every query row gets q_shift * u and key row n gets c_n * u, with u a fixed unit
+    vector, so a score gains about q_shift * c_n * scale, i.e.
+    q_shift * c_n * scale * log2(e) in base-2 units.  mode "growing": c_n rises by
+    growth_log2 base-2 units per key tile of `tile` keys (c_n proportional to
+    n // tile); mode "late_key": only the last key row is shifted, by
+    (N // tile + 1) * growth_log2 base-2 units.  Returns (dq [d], dk [N, d])."""
+    u = planted_direction(d, seed)
+    per_tile = growth_log2 / (q_shift * scale * 1.4426950408889634)
+    c = np.zeros(N, dtype=np.float64)
+    if mode == "growing":
+        c = (np.arange(N) // tile) * per_tile
+    elif mode == "late_key":
+        c[N - 1] = (N // tile + 1) * per_tile
+    else:
+        raise ValueError(mode)
+    dq = (q_shift * u).astype(np.float32)
+    dk = (c[:, None] * u[None, :]).astype(np.float32)
+    return dq, dk
+
+
+def rescale_fa2_inputs(BH: int, N: int, d: int, seed: int, mode: str = "growing"):
+    """fa2_inputs (bf16) with planted_shifts added to Q and K before rounding."""
+    scale = 1.0 / np.sqrt(d)
+    dq, dk = planted_shifts(N, d, scale, seed, mode)
+    out = {}
+    for i, name in enumerate(("q", "k", "v", "do")):
+        x = normal_f32((BH, N, d), seed, 1.0, i)
+        if name == "q":
+            x = x + dq[None, None, :]
+        elif name == "k":
+            x = x + dk[None, :, :]
+        out[name] = f32_to_bf16(x.astype(np.float32))
+    return out
+
+
+def rescale_psa_inputs(B: int, num_heads: int, key_dim: int, H: int, W: int, seed: int,
+                       mode: str = "growing"):
+    """psa_inputs (bf16, with dOut) with planted_shifts added to the Q and K channels
+    of every head (positions n = h*W + w) before rounding."""
+    N, KD = H * W, key_dim
+    scale = 1.0 / np.sqrt(KD)
+    dq, dk = planted_shifts(N, KD, scale, seed, mode)
+    C = num_heads * 4 * KD
+    qkv = normal_f32((B, C, H, W), seed, 1.0, 0).reshape(B, num_heads, 4, KD, N)
+    qkv[:, :, 0] += dq[None, None, :, None]
+    qkv[:, :, 1] += dk.T[None, None, :, :]
+    out = {"qkv": f32_to_bf16(qkv.reshape(B, C, H, W).astype(np.float32))}
+    out["dout"] = f32_to_bf16(normal_f32((B, num_heads * 2 * KD, H, W), seed, 1.0, 1))
+    return out
