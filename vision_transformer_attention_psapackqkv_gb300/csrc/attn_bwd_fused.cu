@@ -20,25 +20,31 @@
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing, the optional
 // PsaExtractV gradient is added into the V channels), as in the split kernels.
 //
-// Fused kernel: one CTA per SM (persistent over heads), 608 threads.  A step is
+// Fused kernel: one CTA per SM (persistent over heads), 768 threads.  A step is
 // (key tile kt of 128 keys, query sub-tile j of 64 queries); dQ is accumulated
 // per 128-query tile, i.e. once every two steps.
 //   warps 0-15 row threads: warp w serves TMEM lanes 32(w%4).. (key rows) and
 //              query columns 16(w/4)..+15 of the step (four warps per SM
 //              sub-partition, so one warp's waits overlap the others'
 //              exponentials); they turn S^T / dP^T into bf16 P^T and dS^T in
-//              shared memory and write dK, dV per key tile and dQ per head;
+//              shared memory, and compute each head's delta at its start;
 //   warp 16    TMA producer (K / V per key tile, double-buffered; Q / dO per step
 //              in a ring; lse2 of a head into shared memory, from registers
 //              loaded one head ahead);
 //   warp 17    issues S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffers
 //              (64 + 64 columns each, by step parity) and owns the 512 columns;
 //   warp 18    issues the gradient products into dV (64 columns), dK (32) and
-//              dQ of up to 4 query tiles (4 x 32).
+//              dQ of up to 4 query tiles (4 x 32);
+//   warp 19    idle;
+//   warps 20-23 epilogue: read dV / dK of a finished key tile out of tensor
+//              memory, hand the accumulators back, and write them to dQKV (with
+//              dVres); read and write dQ once a head is done.
 // With two S^T / dP^T buffers the products of step s+1 run while the row
 // threads work on step s; P^T is double-buffered and dS^T pair-buffered in
 // shared memory, so neither side waits for the other's previous step.  Two
-// issuing threads keep the tensor pipe fed while one of them waits.
+// issuing threads keep the tensor pipe fed while one of them waits.  The row
+// threads never wait for a key tile's products to drain: the epilogue warps do,
+// while the rows already work on the next key tile's first steps.
 //   dV += P^T dO,  dK += dS^T Q  (per step);  dQ_t += dS K  (dS read as the
 //   MN-major view of the two dS^T halves of tile t).
 #include <math.h>
@@ -85,8 +91,10 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[NC], const uint3
 template <int DQK, int DV, int ST>
 struct FusedCfg {
   static constexpr int BK = 128, BQ = 64, QT = 128, MAXN = kFusedBwdMaxN, MAXQT = MAXN / QT;
-  static constexpr int kRowWarps = 16, kThreads = 32 * kRowWarps + 96;
+  static constexpr int kRowWarps = 16, kThreads = 32 * kRowWarps + 256;
   static constexpr int kProducer = kRowWarps, kSIssuer = kRowWarps + 1, kGIssuer = kRowWarps + 2;
+  // four epilogue warps, warp % 4 = TMEM lane quadrant
+  static constexpr int kEpiWarp0 = kRowWarps + 4, kEpiThreads = 128;
   static constexpr uint32_t K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
   static constexpr uint32_t Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
   static constexpr uint32_t STAGE_BYTES = Q_BYTES + DO_BYTES;
@@ -98,20 +106,22 @@ struct FusedCfg {
   static constexpr uint32_t OFF_PT = OFF_STAGE + ST * STAGE_BYTES;  // P^T: two buffers
   static constexpr uint32_t OFF_DST = OFF_PT + 2 * HALF_BYTES;      // dS^T: two pair buffers
   static constexpr uint32_t OFF_HSTAT = OFF_DST + 2 * PAIR_BYTES;  // two heads
-  static constexpr uint32_t OFF_BAR = OFF_HSTAT + 2 * HSTAT_BYTES;
+  static constexpr uint32_t OFF_DSCR = OFF_HSTAT + 2 * HSTAT_BYTES;  // delta partial sums
+  static constexpr uint32_t OFF_BAR = OFF_DSCR + 8 * MAXN * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
   // TMEM columns: S^T_b at 64 b, dP^T_b at 128 + 64 b
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = TM_DV + DV;
   static constexpr uint32_t TM_DQ = TM_DK + DQK;
   static_assert(TM_DQ + MAXQT * DQK <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024 && SMEM_BYTES > 114 * 1024, "one CTA per SM");
+  static_assert(kEpiWarp0 % 4 == 0, "epilogue warps cover the four lane quadrants in order");
   static_assert(ST >= 2 && ST <= 8, "stages");
 };
 
 struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[8], q_empty[8];
   uint64_t s_full[2], s_free[2], p_full[2], g_done[2], hs_full[2], hs_free[2];
-  uint64_t acc_full, acc_free, mma_done[2];
+  uint64_t acc_full, acc_free, dq_full, dq_free, mma_done[2];
   uint64_t dl_part, dl_full;  // a head's delta: partial sums written, delta written
 };
 static_assert(sizeof(FusedBars) + 8 <= 512, "barrier area");
@@ -124,7 +134,7 @@ __device__ __forceinline__ uint64_t off_ch_by_pos(int kk) {
 }
 
 template <int DQK, int DV, int ST>
-__global__ void __launch_bounds__(608, 1)
+__global__ void __launch_bounds__(768, 1)
     attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -167,7 +177,9 @@ __global__ void __launch_bounds__(608, 1)
       mbar_init(&b.q_empty[i], 1);
     }
     mbar_init(&b.acc_full, 1);
-    mbar_init(&b.acc_free, 32 * C::kRowWarps);
+    mbar_init(&b.acc_free, C::kEpiThreads);
+    mbar_init(&b.dq_full, 1);
+    mbar_init(&b.dq_free, C::kEpiThreads);
     mbar_init(&b.dl_part, 32 * C::kRowWarps);
     mbar_init(&b.dl_full, 32 * C::kRowWarps);
     *abort = 0;
@@ -307,8 +319,13 @@ __global__ void __launch_bounds__(608, 1)
       };
       auto issue_grad = [&](int u, int kt, int j) -> bool {
         const int kvi = u * nkt + kt, s = kvi * nqs + j, st = s % ST, kb = kvi & 1, bb = s & 1;
+        // the first dQ product of a head overwrites the accumulators the epilogue
+        // warps read out for the previous head
+        const bool dq_step = (j & 1) || j == nqs - 1;
+        const bool first_dq = kt == 0 && dq_step && j <= 1;
         if (!mbar_wait(&b.p_full[bb], (s >> 1) & 1, abort) ||
-            (j == 0 && kvi >= 1 && !mbar_wait(&b.acc_free, (kvi - 1) & 1, abort)))
+            (j == 0 && kvi >= 1 && !mbar_wait(&b.acc_free, (kvi - 1) & 1, abort)) ||
+            (first_dq && u >= 1 && !mbar_wait(&b.dq_free, (u - 1) & 1, abort)))
           return false;
         tc_fence_after();
         const int qt = j >> 1, pi = kvi * nqt + qt, pb = pi & 1;
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(608, 1)
             mma_bf16(tmem + C::TM_DK, dDST + 2 * kk, dQb + 2 * kk, idDK, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&b.q_empty[st]);
         // dQ of the 128-query tile once both of its halves (or its only one) are stored
-        if ((j & 1) || j == nqs - 1) {
+        if (dq_step) {
           const uint64_t dDS = dDS0 + (uint64_t)(pb * C::PAIR_BYTES >> 4);
           const uint64_t dKb = dKb0 + (uint64_t)(kb * C::K_BYTES >> 4);
 #pragma unroll
@@ -342,6 +359,7 @@ __global__ void __launch_bounds__(608, 1)
         if (j == nqs - 1) {
           mma_commit(&b.kv_empty[kb]);
           mma_commit(&b.acc_full);
+          if (kt == nkt - 1) mma_commit(&b.dq_full);
         }
         return true;
       };
@@ -355,13 +373,81 @@ __global__ void __launch_bounds__(608, 1)
       mma_commit(&b.mma_done[warp - C::kSIssuer]);
       drain_wait(&b.mma_done[warp - C::kSIssuer], 0);
     }
-  } else {
+  } else if (warp >= C::kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue warps
+    // One thread per TMEM lane (key row of dV / dK, query row of a dQ tile).
+    const int wl = warp & 3;
+    const int r = wl * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
+    const float sc = args.scale;
+    bool ok = true;
+    for (int u = 0; ok && u < nunits; ++u) {
+      const int bh = head_of(u);
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int kvi = u * nkt + kt;
+        if (!mbar_wait(&b.acc_full, kvi & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dV (column groups 0, 1: 32 channels each) and dK (group 2) of this key
+        // tile's rows, one group at a time; the accumulators go back to the
+        // gradient issuer as soon as the last group is in registers
+        const int key = kt * C::BK + r;
+        const bool live = key < N;
+#pragma unroll 1
+        for (int g = 0; g < 3; ++g) {
+          float acc[32];
+          tmem_load32(tmem + lane_base + C::TM_DV + 32 * g, acc);  // dK follows dV's 64 columns
+          if (g == 2) {
+            tc_fence_before();
+            mbar_arrive(&b.acc_free);
+          }
+          if (!live) continue;
+          if (g < 2) {
+            __nv_bfloat16* dst = args.dv + ((long long)qkv_row(bh) + 2 * DQK + 32 * g) * N + key;
+            const __nv_bfloat16* res =
+                args.dvres ? args.dvres + ((long long)out_row(bh) + 32 * g) * N + key : nullptr;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float x = acc[e];
+              if (res) x += bf(res[(long long)e * N]);
+              dst[(long long)e * N] = __float2bfloat16_rn(x);
+            }
+          } else {
+            __nv_bfloat16* dst = args.dk + ((long long)qkv_row(bh) + DQK) * N + key;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
+          }
+        }
+      }
+      if (!ok) break;
+      // the head's last products are done: dQ of every 128-query tile
+      if (!mbar_wait(&b.dq_full, u & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int qt = 0; qt < nqt; ++qt) {
+        const int q = qt * C::QT + r;
+        float acc[32];
+        tmem_load32(tmem + lane_base + C::TM_DQ + qt * DQK, acc);
+        if (q < N) {
+          __nv_bfloat16* dst = args.dq + (long long)qkv_row(bh) * N + q;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&b.dq_free);
+    }
+  } else if (warp < C::kRowWarps) {
     // ------------------------------------------------------------ row threads
     const int wl = warp & 3, cq = warp >> 2;
     const int r = wl * 32 + lane;  // TMEM lane: key row of S^T, query row of dQ
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
     const int c0 = cq * 16;        // first query column of this thread in a step
-    const float sl2 = args.scale_log2, sc = args.scale;
+    const float sl2 = args.scale_log2;
     bool ok = true;
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
@@ -369,9 +455,8 @@ __global__ void __launch_bounds__(608, 1)
       {
         // delta[q] = sum_c Out[c, q] dOut[c, q] over the head's DV channels, while
         // its first tiles load.  Thread t = 64 s + g sums channels 8s .. 8s+7 at
-        // positions 8g .. 8g+7; the eight channel slices meet in the P^T buffers,
-        // idle here (every product of the previous head has completed: its last
-        // dV / dK epilogue waited for them).
+        // positions 8g .. 8g+7; the eight channel slices meet in a scratch area
+        // of shared memory.
         static_assert(C::kRowWarps * 32 == C::MAXN && DV == 64, "one thread per 8 x 8 block");
         const int t = threadIdx.x, g = t & 63, sl8 = t >> 6;
         float part[8];
@@ -398,7 +483,7 @@ __global__ void __launch_bounds__(608, 1)
             }
           }
         }
-        float* scratch = reinterpret_cast<float*>(smem + C::OFF_PT);
+        float* scratch = reinterpret_cast<float*>(smem + C::OFF_DSCR);
         float4* sp = reinterpret_cast<float4*>(scratch + sl8 * C::MAXN + 8 * g);
         sp[0] = make_float4(part[0], part[1], part[2], part[3]);
         sp[1] = make_float4(part[4], part[5], part[6], part[7]);
@@ -479,63 +564,6 @@ __global__ void __launch_bounds__(608, 1)
           mbar_arrive(&b.p_full[bb]);
         }
         if (!ok) break;
-        // ---- key tile done: dV (column groups 0, 1: 32 channels each) and dK
-        // (column group 2) of its keys
-        if (!mbar_wait(&b.acc_full, kvi & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (krows && cq < 3) {
-          const int key = kt * C::BK + r;
-          const bool live = key < N;
-          float acc[32];
-          if (cq < 2) {
-            const int c = 32 * cq;
-            tmem_load32(tmem + lane_base + C::TM_DV + c, acc);
-            if (live) {
-              __nv_bfloat16* dst = args.dv + ((long long)qkv_row(bh) + 2 * DQK + c) * N + key;
-              const __nv_bfloat16* res =
-                  args.dvres ? args.dvres + ((long long)out_row(bh) + c) * N + key : nullptr;
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                float x = acc[e];
-                if (res) x += bf(res[(long long)e * N]);
-                dst[(long long)e * N] = __float2bfloat16_rn(x);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < DQK; c += 32) {
-              tmem_load32(tmem + lane_base + C::TM_DK + c, acc);
-              if (live) {
-                __nv_bfloat16* dst = args.dk + ((long long)qkv_row(bh) + DQK + c) * N + key;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
-              }
-            }
-          }
-        }
-        // ---- last key tile of the head: dQ of every 128-query tile (column
-        // group g takes query tiles g, g + 4, ...)
-        if (kt == nkt - 1) {
-          for (int qt = cq; qt < nqt; qt += 4) {
-            if (wl * 32 >= N - qt * C::QT) continue;
-            const int q = qt * C::QT + r;
-            float acc[32];
-#pragma unroll
-            for (int c = 0; c < DQK; c += 32) {
-              tmem_load32(tmem + lane_base + C::TM_DQ + qt * DQK + c, acc);
-              if (q < N) {
-                __nv_bfloat16* dst = args.dq + ((long long)qkv_row(bh) + c) * N + q;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
-              }
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&b.acc_free);
       }
       mbar_arrive(&b.hs_free[u & 1]);
     }

@@ -15,8 +15,8 @@
 //                      and a 2- to 4-stage ring of 64-key K/V tiles
 //   warp P + 1         MMA issuer (one thread) and TMEM owner; per slot
 //                        S_k = Q K_k^T -> TMEM (64 columns)
-//                        O  += P_k V_k -> TMEM (DV columns), P_k from shared
-//                        memory (double-buffered)
+//                        O  += P_k V_k -> TMEM (DV columns), P_k read from
+//                        tensor memory (A operand; double-buffered)
 //                      S_{k+1} is issued as soon as the softmax holds S_k in
 //                      registers, so it overlaps the exponentials of tile k.
 // The bf16 kernels run persistent grids; with one slot per CTA two CTAs share
@@ -29,7 +29,9 @@
 // start (programmatic dependent launch) and waits for the previous one before
 // touching global memory.
 // Softmax: running max in the log2 domain; p = 2^(scale*log2e*s - m) rounded to
-// bf16 into P (K-major, 128-byte swizzle); O is rescaled in TMEM only when a row
+// bf16 and written by each thread into its own TMEM lane (two per 32-bit column),
+// where the P.V product reads it as its A operand, so P never passes through
+// shared memory; O is rescaled in TMEM only when a row
 // max grows by more than 2^8 (exact either way, since O and the running sum
 // share the stale max).  Epilogue: O / l in the output layout and the LSE.
 // Layouts: kNCHW = false reads [BH, N, D] planes (Q, K K-major; V MN-major);
@@ -72,22 +74,23 @@ struct FwdCfg {
   static constexpr uint32_t Q_BYTES = BM * DQK * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2;
   static constexpr uint32_t V_BYTES = BN * DV * 2;
-  static constexpr uint32_t P_BYTES = BM * BN * 2;
   // per-slot shared memory region
   static constexpr uint32_t SL_Q = 0;
   static constexpr uint32_t SL_K = SL_Q + QBUF * Q_BYTES;
   static constexpr uint32_t SL_V = SL_K + STAGES * K_BYTES;
-  static constexpr uint32_t SL_P = SL_V + STAGES * V_BYTES;
   // split rows: per tile parity, (max, sum) of both halves of every row
-  static constexpr uint32_t SL_ML = SL_P + 2 * P_BYTES;  // P double-buffered
+  static constexpr uint32_t SL_ML = SL_V + STAGES * V_BYTES;
   static constexpr uint32_t SL_BYTES = SL_ML + (kSplit ? 2 * 2 * BM * 8 : 0);
   static constexpr uint32_t OFF_BAR = NWG * SL_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
   // tensor memory per slot w: S (BN columns) at TM_SLOT * w, then H O accumulators
-  // (DV columns each; accumulator h sums the P.V products of key half h)
+  // (DV columns each; accumulator h sums the P.V products of key half h), then P
+  // in two buffers of BN / 2 columns (bf16 pairs)
   static constexpr uint32_t TM_O = BN;
-  static constexpr uint32_t TM_SLOT = (BN + H * DV <= 128) ? 128 : 256;
-  static_assert(BN + H * DV <= 256, "tensor memory per slot");
+  static constexpr uint32_t TM_P = BN + H * DV;
+  static constexpr uint32_t TM_SLOT = (TM_P + BN <= 128) ? 128 : 256;
+  static_assert(TM_P + BN <= 256, "tensor memory per slot");
+  static_assert(SL_ML % 1024 == 0, "1024-byte aligned (max, sum) area");
   static constexpr uint32_t TMEM_COLS = NWG * TM_SLOT < 32 ? 32 : NWG * TM_SLOT;
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(DQK % 16 == 0 && DV % 32 == 0 && DV <= 128, "tile shape");
@@ -335,10 +338,9 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
       // descriptors of buffer 0 / stage 0 of slot 0; the others are fixed offsets
       const uint64_t dQ0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_Q, C::BM), 0);
       const uint64_t dK0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_K, C::BN), 0);
-      const uint64_t dP0 = desc_kmajor(SmemTile{sbase + C::SL_P, 128, C::BM}, 0);
       const uint64_t dV0 = desc_ch_by_pos<kNCHW>(tile_view<kNCHW, DV>(sbase + C::SL_V, C::BN), 0);
       constexpr uint64_t kStepQK = kstep_pos_by_ch<kNCHW, DQK>();
-      constexpr uint64_t kStepP = 32 >> 4, kStepV = kstep_ch_by_pos<kNCHW, DV>();
+      constexpr uint64_t kStepV = kstep_ch_by_pos<kNCHW, DV>();
       const uint32_t idS_full = idesc_bf16_f32(128, C::BN, kNCHW, kNCHW);
       const uint32_t idPV = idesc_bf16_f32(128, DV, false, !kNCHW);
       auto issue_s = [&](int w, int i, int j) -> bool {
@@ -371,7 +373,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
           return false;
         tc_fence_after();
         const uint64_t slot_off = (uint64_t)(w * C::SL_BYTES) >> 4;
-        const uint64_t dP = dP0 + slot_off + (uint64_t)((k & 1) * C::P_BYTES >> 4);
+        // P of this tile: 8 TMEM columns (16 keys) per k-step
+        const uint32_t tP = tmem + w * C::TM_SLOT + C::TM_P + (k & 1) * (C::BN / 2);
         const uint64_t dV = dV0 + slot_off + (uint64_t)((k % C::STAGES) * C::V_BYTES >> 4);
         const uint32_t tO = tmem + w * C::TM_SLOT + C::TM_O;
         const int valid = min(C::BN, N - j * C::BN);
@@ -380,12 +383,12 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
         if (valid == C::BN) {
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_bf16(tO + (kk / KH) * DV, dP + kk * kStepP, dV + kk * kStepV, idPV,
-                     (j > 0 || kk % KH > 0) ? 1u : 0u);
+            mma_bf16_ts(tO + (kk / KH) * DV, tP + kk * 8, dV + kk * kStepV, idPV,
+                        (j > 0 || kk % KH > 0) ? 1u : 0u);
         } else {
           for (int kk = 0; kk * 16 < valid; ++kk)
-            mma_bf16(tO + (kk / KH) * DV, dP + kk * kStepP, dV + kk * kStepV, idPV,
-                     (j > 0 || kk % KH > 0) ? 1u : 0u);
+            mma_bf16_ts(tO + (kk / KH) * DV, tP + kk * 8, dV + kk * kStepV, idPV,
+                        (j > 0 || kk % KH > 0) ? 1u : 0u);
         }
         mma_commit(&b.pv_done[k & 1]);
         mma_commit(&b.kv_empty[k % C::STAGES]);
@@ -486,14 +489,12 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
         }
         tc_fence_after();
         if (active) {
-          const uint32_t pbuf = sl + C::SL_P + (k & 1) * C::P_BYTES;
+          // this thread's P (keys >= N already zeroed) into its TMEM lane, beside
+          // the other half's
+          const uint32_t tP = tS + C::TM_P + (k & 1) * (C::BN / 2) + h * (C::HC / 2) + lane_base;
 #pragma unroll
-          for (int ch = 0; ch < C::HC / 8; ++ch) {
-            const int gch = h * (C::HC / 8) + ch;  // 16-byte chunk within the P row
-            if (ch * 8 < kend)
-              st_shared_v4(pbuf + (gch >> 3) * (C::BM * 128) + swizzled_offset(r, gch & 7, 128),
-                           s[ch * 4], s[ch * 4 + 1], s[ch * 4 + 2], s[ch * 4 + 3]);
-          }
+          for (int c = 0; c < C::HC / 2; c += 16) tmem_store16_async(tP + c, s + c);
+          tmem_wait_st();
           // O may only be rescaled once every earlier P.V has landed in it
           if (__any_sync(0xffffffffu, alpha != 1.f) &&
               !mbar_wait(&b.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort)) {
@@ -512,7 +513,6 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
             }
           }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&b.p_full[k & 1]);
       }
