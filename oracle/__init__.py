@@ -59,6 +59,7 @@ def _load():
         lib.oracle_attn_bwd_dkdv_rows.argtypes = [P, P, P, P, I, I, I, D, P, I, P, P, I]
         lib.oracle_psa_fwd.argtypes = [P, P, P, P, I, I, I, I, D, I]
         lib.oracle_psa_bwd.argtypes = [P, P, P, P, I, I, I, I, D, I]
+        lib.oracle_psa_fwd_residual.argtypes = [P, P, P, I, I, I, I, D, I]
         _lib = lib
     return _lib
 
@@ -203,6 +204,19 @@ def psa_fwd(qkv, num_heads: int, key_dim: int, scale: float, nthreads: int | Non
     _load().oracle_psa_fwd(_ptr(qkv), _ptr(out), _ptr(lse), _ptr(vres), B, num_heads, key_dim,
                            H * W, float(scale), nthreads or default_threads())
     return out, lse, vres
+
+
+def psa_fwd_residual(qkv, num_heads: int, key_dim: int, scale: float, nthreads: int | None = None):
+    """PSA forward with its residual path added (float64): returns out + vres
+    [B, nh*2KD, H, W] and LSE [B*nh, H*W]."""
+    qkv = _c(qkv, np.float64)
+    B, C, H, W = qkv.shape
+    assert C == num_heads * 4 * key_dim
+    out = np.empty((B, num_heads * 2 * key_dim, H, W))
+    lse = np.empty((B * num_heads, H * W))
+    _load().oracle_psa_fwd_residual(_ptr(qkv), _ptr(out), _ptr(lse), B, num_heads, key_dim, H * W,
+                                    float(scale), nthreads or default_threads())
+    return out, lse
 
 
 def psa_bwd(qkv, dout, num_heads: int, key_dim: int, scale: float, dvres=None,

@@ -436,6 +436,26 @@ void oracle_psa_fwd(const double *qkv, double *out, double *lse, double *vres, i
 
 /* Backward of the chain above: dqkv = d(sum(dout o out) + sum(dvres o vres)) / dqkv,
  * obtained by running each step's adjoint in reverse order (dvres may be NULL). */
+/* The attention output with its residual path added: out_res = out + vres, where
+ * out is the merged attention output and vres the PsaExtractV output of
+ * oracle_psa_fwd (page "Custom Kernels", section "Position-Sensitive Attention
+ * (PSA)": PsaExtractV pulls the V section out in NCHW for the residual path; the
+ * reading taken is that this path adds it, element by element, to the merged
+ * attention output of the same shape).  lse may be NULL. */
+void oracle_psa_fwd_residual(const double *qkv, double *out_res, double *lse, int B, int nh,
+                             int KD, int N, double scale, int nthreads)
+{
+    const long n = (long)B * nh * 2 * KD * N;
+    double *v = (double *)malloc(sizeof(double) * (size_t)n);
+    double *lse_buf = lse ? lse : (double *)malloc(sizeof(double) * (size_t)((long)B * nh * N));
+    oracle_psa_fwd(qkv, out_res, lse_buf, v, B, nh, KD, N, scale, nthreads);
+    for (long i = 0; i < n; ++i)
+        out_res[i] = out_res[i] + v[i];
+    if (!lse)
+        free(lse_buf);
+    free(v);
+}
+
 void oracle_psa_bwd(const double *qkv, const double *dout, const double *dvres, double *dqkv,
                     int B, int nh, int KD, int N, double scale, int nthreads)
 {
