@@ -130,6 +130,19 @@ psa_status_t flash_attn2_bwd_dkdv(const void *q, const void *k, const void *v, c
 psa_status_t psa_attention_fwd(const void *qkv_nchw, void *out_nchw, float *lse, void *v_nchw,
                                psa_shape_t shape, float scale, cudaStream_t stream);
 
+/* The same forward with the residual path fused into its epilogue
+ * ("Custom Kernels", section "Position-Sensitive Attention (PSA)": PsaExtractV
+ * pulls the V section out in NCHW for the residual path, which adds it to the
+ * merged attention output): writes out_res [B, c, H, W] = Out + V, each element
+ * rounded once, where V is the PsaExtractV output; also writes the plain attention
+ * output out and lse [BH, N] when they are not NULL.  The backward of out_res is
+ * psa_attention_bwd with dvres_nchw = dout_nchw (the residual adds the upstream
+ * gradient into the V channels); it needs out, so callers that train pass out here.
+ * Same sizes, dtypes and errors as psa_attention_fwd (out_res is required). */
+psa_status_t psa_attention_fwd_residual(const void *qkv_nchw, void *out_res_nchw, void *out_nchw,
+                                        float *lse, psa_shape_t shape, float scale,
+                                        cudaStream_t stream);
+
 /* Backward of psa_attention_fwd: given qkv, the forward's out and lse, the
  * upstream gradient dout [B, c, H, W] and optionally the gradient dvres of the
  * extracted V (nullable), writes dqkv_nchw [B, qkv_h, H, W] (overwritten, V

@@ -140,3 +140,14 @@ def test_debug_wait_limit_validation(lib):
     # rejected before any launch: the limit must lie in 1 ns .. 100 ms
     assert lib.psa_debug_wait_timeout(0, None) == INVALID
     assert lib.psa_debug_wait_timeout(100_000_001, None) == INVALID
+
+
+@placeholder_only
+def test_residual_forward_validation(lib):
+    f = lib.psa_attention_fwd_residual
+    assert f(A, None, A, None, _shape(), 0.17, None) == INVALID          # out_res required
+    assert f(None, A, None, None, _shape(), 0.17, None) == INVALID       # qkv required
+    assert f(A, MIS, None, None, _shape(), 0.17, None) == ALIGNMENT
+    assert f(A, A, MIS, None, _shape(), 0.17, None) == ALIGNMENT
+    assert f(A, A, None, None, _shape(KD=16), 0.17, None) == UNSUPPORTED
+    assert f(A, A, None, None, _shape(H=3, W=3), 0.17, None) == ALIGNMENT

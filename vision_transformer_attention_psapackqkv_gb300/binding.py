@@ -34,7 +34,7 @@ class PsaShape(ctypes.Structure):
 EXPORTED = (
     "psa_pack_qkv", "psa_unpack_qkv", "psa_extract_v", "psa_merge_attn", "psa_unmerge_attn",
     "flash_attn2_fwd", "flash_attn2_bwd_dq", "flash_attn2_bwd_dkdv", "psa_attention_fwd",
-    "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv", "psa_attention_bwd_noalloc",
+    "psa_attention_fwd_residual", "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv", "psa_attention_bwd_noalloc",
     "psa_attention_bwd_workspace_size", "psa_status_string",
     "psa_get_last_device_error", "psa_debug_wait_timeout",
 )
@@ -64,6 +64,7 @@ def load(path: str | None = None):
         "flash_attn2_bwd_dq": [P, P, P, P, P, P, P, P, I, I, I, F, I, P],
         "flash_attn2_bwd_dkdv": [P, P, P, P, P, P, P, P, I, I, I, F, I, P],
         "psa_attention_fwd": [P, P, P, P, S, F, P],
+        "psa_attention_fwd_residual": [P, P, P, P, S, F, P],
         "psa_attention_bwd": [P, P, P, P, P, P, P, Z, S, F, P],
         "psa_attention_bwd_dq": [P, P, P, P, P, P, S, F, P],
         "psa_attention_bwd_dkdv": [P, P, P, P, P, P, S, F, P],
@@ -165,6 +166,11 @@ def flash_attn2_bwd_dkdv(q, k, v, do, lse, delta, dk, dv, scale: float, stream=N
 def psa_attention_fwd(qkv, out, lse, v_nchw, shape: PsaShape, scale: float, stream=None):
     _check("psa_attention_fwd", load().psa_attention_fwd(
         _ptr(qkv), _ptr(out), _ptr(lse), _ptr(v_nchw), shape, float(scale), _stream(stream)))
+
+
+def psa_attention_fwd_residual(qkv, out_res, out, lse, shape: PsaShape, scale: float, stream=None):
+    _check("psa_attention_fwd_residual", load().psa_attention_fwd_residual(
+        _ptr(qkv), _ptr(out_res), _ptr(out), _ptr(lse), shape, float(scale), _stream(stream)))
 
 
 def psa_attention_bwd_workspace_size(shape: PsaShape) -> int:

@@ -313,23 +313,26 @@ psa_status_t flash_attn2_bwd_dkdv(const void* q, const void* k, const void* v, c
 }
 
 // ---------------------------------------------------------------- fused PSA
-psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_nchw,
-                               psa_shape_t s, float scale, cudaStream_t st) {
-  if (!qkv || !out) return PSA_ERR_INVALID_ARG;
+namespace {
+// The forward kernels write any of out, lse, v_nchw (PsaExtractV) and out_res
+// (out + V) that is not null; at least one of out, out_res is required.
+psa_status_t fused_fwd(const void* qkv, void* out, float* lse, void* v_nchw, void* out_res,
+                       psa_shape_t s, float scale, cudaStream_t st) {
+  if (!qkv || (!out && !out_res)) return PSA_ERR_INVALID_ARG;
   psa_status_t e = check_shape(s);
   if (e != PSA_OK) return e;
   if (!isfinite(scale) || !(scale > 0.f)) return PSA_ERR_INVALID_ARG;
   if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
   if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;
-  if (!aligned16(qkv) || !aligned16(out) || (lse && !aligned16(lse)) ||
-      (v_nchw && !aligned16(v_nchw)))
+  if (!aligned16(qkv) || (out && !aligned16(out)) || (lse && !aligned16(lse)) ||
+      (v_nchw && !aligned16(v_nchw)) || (out_res && !aligned16(out_res)))
     return PSA_ERR_ALIGNMENT;
   const int N = s.H * s.W;
   if (((long long)N * elem_bytes(s.dtype)) % 16 != 0) return PSA_ERR_ALIGNMENT;
   const int nh = s.num_heads, KD = s.key_dim;
   if (s.dtype == PSA_DTYPE_F32) {
-    e = from_cuda(psa::launch_psa_fwd_f32((const float*)qkv, (float*)out, lse, s.B, nh, KD, N,
-                                          scale, st));
+    e = from_cuda(psa::launch_psa_fwd_f32((const float*)qkv, (float*)out, (float*)out_res, lse,
+                                          s.B, nh, KD, N, scale, st));
   } else {
     CUtensorMap mqk, mv;
     const long long rows = (long long)s.B * nh * 4 * KD;
@@ -346,10 +349,25 @@ psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_n
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
     a.vres = static_cast<__nv_bfloat16*>(v_nchw);  // PsaExtractV fused into the forward
+    a.out_res = static_cast<__nv_bfloat16*>(out_res);
+    a.qkv = static_cast<const __nv_bfloat16*>(qkv);
     return from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, a, KD, st));
   }
   if (e != PSA_OK || !v_nchw) return e;
   return from_cuda(psa::launch_extract_v(qkv, v_nchw, s.B, nh, KD, N, elem_bytes(s.dtype), st));
+}
+}  // namespace
+
+psa_status_t psa_attention_fwd(const void* qkv, void* out, float* lse, void* v_nchw,
+                               psa_shape_t s, float scale, cudaStream_t st) {
+  if (!out) return PSA_ERR_INVALID_ARG;
+  return fused_fwd(qkv, out, lse, v_nchw, nullptr, s, scale, st);
+}
+
+psa_status_t psa_attention_fwd_residual(const void* qkv, void* out_res, void* out, float* lse,
+                                        psa_shape_t s, float scale, cudaStream_t st) {
+  if (!out_res) return PSA_ERR_INVALID_ARG;
+  return fused_fwd(qkv, out, lse, nullptr, out_res, s, scale, st);
 }
 
 size_t psa_attention_bwd_workspace_size(psa_shape_t s) {

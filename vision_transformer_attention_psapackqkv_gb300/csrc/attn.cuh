@@ -14,9 +14,13 @@ struct FwdArgs {
   int out_ch;        // channels per batch of the output (NCHW layout)
   int vres_ch;       // channels per batch of the extracted V (NCHW layout)
   float scale_log2;  // scale * log2(e), > 0
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;   // may be null when out_res is not
   float* lse;        // [BH, N] natural-log LSE, may be null
   __nv_bfloat16* vres;  // NCHW: PsaExtractV output [B, vres_ch, N], may be null
+  // NCHW residual path: out_res = Out + V (V read from qkv at the query
+  // positions), written when not null
+  __nv_bfloat16* out_res;
+  const __nv_bfloat16* qkv;
 };
 
 // bf16 tcgen05 forward, persistent grid.  Raw: 3-D maps over [BH, N, d] (box {d, 128, 1}).
@@ -29,8 +33,8 @@ cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
 
 cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
                                float* lse, int BH, int N, int d, float scale, cudaStream_t st);
-cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, int nh, int KD,
-                               int N, float scale, cudaStream_t st);
+cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* out_res, float* lse, int B,
+                               int nh, int KD, int N, float scale, cudaStream_t st);
 
 // Launches kern with programmatic stream serialization: its CTAs may become
 // resident and run their prologue (barrier set-up, tensor memory allocation)

@@ -561,10 +561,21 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
                               : __uint_as_float(a0[e]) * c0s;
             if (live) {
               if (kNCHW) {
-                __nv_bfloat16* dst = args.out +
+                const long long orow =
                     ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + ch) * N + q;
+                if (args.out) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dst[(long long)e * N] = __float2bfloat16_rn(o[e]);
+                  for (int e = 0; e < 16; ++e)
+                    args.out[orow + (long long)e * N] = __float2bfloat16_rn(o[e]);
+                }
+                if (args.out_res) {
+                  const __nv_bfloat16* vsrc = args.qkv + ((long long)(bh / args.nh) * args.qkv_ch +
+                                                          (bh % args.nh) * 4 * DQK + 2 * DQK + ch) * N + q;
+#pragma unroll
+                  for (int e = 0; e < 16; ++e)
+                    args.out_res[orow + (long long)e * N] =
+                        __float2bfloat16_rn(o[e] + __bfloat162float(vsrc[(long long)e * N]));
+                }
               } else {
                 uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + ch);
 #pragma unroll
@@ -588,10 +599,21 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
           tmem_load32(tO + lane_base + c, o);
           if (live) {
             if (kNCHW) {
-              __nv_bfloat16* dst = args.out +
+              const long long orow =
                   ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + c) * N + q;
+              if (args.out) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(o[e] * inv_l);
+                for (int e = 0; e < 32; ++e)
+                  args.out[orow + (long long)e * N] = __float2bfloat16_rn(o[e] * inv_l);
+              }
+              if (args.out_res) {
+                const __nv_bfloat16* vsrc = args.qkv + ((long long)(bh / args.nh) * args.qkv_ch +
+                                                        (bh % args.nh) * 4 * DQK + 2 * DQK + c) * N + q;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  args.out_res[orow + (long long)e * N] =
+                      __float2bfloat16_rn(o[e] * inv_l + __bfloat162float(vsrc[(long long)e * N]));
+              }
             } else {
               uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + c);
 #pragma unroll
@@ -623,8 +645,8 @@ template <int DQK, int DV, bool kNCHW>
 __global__ void __launch_bounds__(128)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                         const float* __restrict__ v, float* __restrict__ out,
-                        float* __restrict__ lse, int N, int nh, int qkv_ch, int out_ch,
-                        float scale) {
+                        float* __restrict__ out_res, float* __restrict__ lse, int N, int nh,
+                        int qkv_ch, int out_ch, float scale) {
   constexpr int TK = 32;
   __shared__ float sk[TK][DQK];
   __shared__ float sv[TK][DV];
@@ -682,10 +704,13 @@ __global__ void __launch_bounds__(128)
   if (i >= N) return;
   const float inv_l = 1.f / l;
   for (int c = 0; c < DV; ++c) {
-    if (kNCHW)
-      out[((long long)b * out_ch + hd * DV + c) * N + i] = acc[c] * inv_l;
-    else
+    if (kNCHW) {
+      const long long o = ((long long)b * out_ch + hd * DV + c) * N + i;
+      if (out) out[o] = acc[c] * inv_l;
+      if (out_res) out_res[o] = acc[c] * inv_l + at(v, 2, i, c, DV);  // Out + V
+    } else {
       out[((long long)bh * N + i) * DV + c] = acc[c] * inv_l;
+    }
   }
   if (lse) lse[(long long)bh * N + i] = m + logf(l);
 }
@@ -708,12 +733,12 @@ cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUten
 }
 
 template <int DQK, int DV, bool kNCHW>
-cudaError_t launch_f32(const float* q, const float* k, const float* v, float* out, float* lse,
-                       int BH, int N, int nh, int qkv_ch, int out_ch, float scale,
-                       cudaStream_t st) {
+cudaError_t launch_f32(const float* q, const float* k, const float* v, float* out,
+                       float* out_res, float* lse, int BH, int N, int nh, int qkv_ch, int out_ch,
+                       float scale, cudaStream_t st) {
   dim3 grid((N + 127) / 128, BH);
-  attn_fwd_f32_kernel<DQK, DV, kNCHW><<<grid, 128, 0, st>>>(q, k, v, out, lse, N, nh, qkv_ch,
-                                                          out_ch, scale);
+  attn_fwd_f32_kernel<DQK, DV, kNCHW><<<grid, 128, 0, st>>>(q, k, v, out, out_res, lse, N, nh,
+                                                          qkv_ch, out_ch, scale);
   return cudaGetLastError();
 }
 
@@ -743,18 +768,18 @@ cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
 
 cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
                                float* lse, int BH, int N, int d, float scale, cudaStream_t st) {
-  if (d == 32) return launch_f32<32, 32, false>(q, k, v, o, lse, BH, N, 1, 0, 0, scale, st);
-  return launch_f32<64, 64, false>(q, k, v, o, lse, BH, N, 1, 0, 0, scale, st);
+  if (d == 32) return launch_f32<32, 32, false>(q, k, v, o, nullptr, lse, BH, N, 1, 0, 0, scale, st);
+  return launch_f32<64, 64, false>(q, k, v, o, nullptr, lse, BH, N, 1, 0, 0, scale, st);
 }
 
-cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* lse, int B, int nh, int KD,
-                               int N, float scale, cudaStream_t st) {
+cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* out_res, float* lse, int B,
+                               int nh, int KD, int N, float scale, cudaStream_t st) {
   const int BH = B * nh;
   if (KD == 32)
-    return launch_f32<32, 64, true>(qkv, qkv, qkv, out, lse, BH, N, nh, nh * 4 * KD,
+    return launch_f32<32, 64, true>(qkv, qkv, qkv, out, out_res, lse, BH, N, nh, nh * 4 * KD,
                                     nh * 2 * KD, scale, st);
-  return launch_f32<64, 128, true>(qkv, qkv, qkv, out, lse, BH, N, nh, nh * 4 * KD, nh * 2 * KD,
-                                   scale, st);
+  return launch_f32<64, 128, true>(qkv, qkv, qkv, out, out_res, lse, BH, N, nh, nh * 4 * KD,
+                                   nh * 2 * KD, scale, st);
 }
 
 }  // namespace psa
