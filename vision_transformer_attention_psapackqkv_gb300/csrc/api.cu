@@ -241,9 +241,12 @@ psa_status_t flash_attn2_fwd(const void* q, const void* k, const void* v, void* 
   psa_status_t e = check_fa2(ptrs, 4, BH, n_ctx, head_dim, scale, dtype);
   if (e != PSA_OK) return e;
   if (lse && !aligned16(lse)) return PSA_ERR_ALIGNMENT;
-  if (dtype == PSA_DTYPE_F32)
-    return from_cuda(psa::launch_fa2_fwd_f32((const float*)q, (const float*)k, (const float*)v,
-                                             (float*)o, lse, BH, n_ctx, head_dim, scale, st));
+  if (dtype == PSA_DTYPE_F32) {
+    psa::SimtArgs a{};
+    a.q = q; a.k = k; a.v = v; a.out = o; a.lse = lse;
+    a.N = n_ctx; a.BH = BH; a.nh = 1; a.scale = scale;
+    return from_cuda(psa::launch_simt_fwd(a, false, false, head_dim, st));
+  }
   CUtensorMap mq, mk, mv;
   // the forward walks 128-query tiles against 64-key tiles
   if (!map_rows(&mq, q, BH, n_ctx, head_dim, 128) || !map_rows(&mk, k, BH, n_ctx, head_dim, 64) ||
@@ -266,7 +269,13 @@ psa_status_t flash_attn2_bwd_dq(const void* q, const void* k, const void* v, con
   const void* ptrs[8] = {q, k, v, o, do_, lse, delta, dq};
   psa_status_t e = check_fa2(ptrs, 8, BH, n_ctx, head_dim, scale, dtype);
   if (e != PSA_OK) return e;
-  if (dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
+  if (dtype == PSA_DTYPE_F32) {
+    psa::SimtArgs a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.dO = do_; a.dq = dq;
+    a.lse = const_cast<float*>(lse); a.delta = delta;
+    a.N = n_ctx; a.BH = BH; a.nh = 1; a.scale = scale;
+    return from_cuda(psa::launch_simt_bwd_dq(a, false, false, head_dim, st));
+  }
   CUtensorMap mq, mk, mv, mdo;
   // the dQ kernel walks 128-query tiles against 64-key tiles
   if (!map_rows(&mq, q, BH, n_ctx, head_dim, 128) || !map_rows(&mk, k, BH, n_ctx, head_dim, 64) ||
@@ -293,7 +302,13 @@ psa_status_t flash_attn2_bwd_dkdv(const void* q, const void* k, const void* v, c
   const void* ptrs[8] = {q, k, v, do_, lse, delta, dk, dv};
   psa_status_t e = check_fa2(ptrs, 8, BH, n_ctx, head_dim, scale, dtype);
   if (e != PSA_OK) return e;
-  if (dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
+  if (dtype == PSA_DTYPE_F32) {
+    psa::SimtArgs a{};
+    a.q = q; a.k = k; a.v = v; a.dO = do_; a.dk = dk; a.dv = dv;
+    a.lse = const_cast<float*>(lse); a.delta = const_cast<float*>(delta);
+    a.N = n_ctx; a.BH = BH; a.nh = 1; a.scale = scale;
+    return from_cuda(psa::launch_simt_bwd_dkdv(a, false, false, head_dim, st));
+  }
   CUtensorMap mq, mk, mv, mdo;
   // the dK/dV kernel walks 128-key tiles against 64-query tiles
   if (!map_rows(&mq, q, BH, n_ctx, head_dim, 64) || !map_rows(&mk, k, BH, n_ctx, head_dim, 128) ||
@@ -314,6 +329,24 @@ psa_status_t flash_attn2_bwd_dkdv(const void* q, const void* k, const void* v, c
 
 // ---------------------------------------------------------------- fused PSA
 namespace {
+// NCHW channel rows of N bf16 elements start on 16-byte boundaries, as the TMA
+// tensor maps of the tensor-core kernels require.
+bool tma_rows(const psa_shape_t& s) { return ((long long)s.H * s.W * 2) % 16 == 0; }
+
+// Arguments of the CUDA-core kernels for an NCHW problem (inputs and outputs set
+// by the caller).
+psa::SimtArgs simt_nchw(const void* qkv, const psa_shape_t& s, float scale) {
+  psa::SimtArgs a{};
+  a.q = a.k = a.v = qkv;
+  a.N = s.H * s.W;
+  a.BH = s.B * s.num_heads;
+  a.nh = s.num_heads;
+  a.qkv_ch = s.num_heads * 4 * s.key_dim;
+  a.out_ch = s.num_heads * 2 * s.key_dim;
+  a.scale = scale;
+  return a;
+}
+
 // The forward kernels write any of out, lse, v_nchw (PsaExtractV) and out_res
 // (out + V) that is not null; at least one of out, out_res is required.
 psa_status_t fused_fwd(const void* qkv, void* out, float* lse, void* v_nchw, void* out_res,
@@ -328,11 +361,14 @@ psa_status_t fused_fwd(const void* qkv, void* out, float* lse, void* v_nchw, voi
       (v_nchw && !aligned16(v_nchw)) || (out_res && !aligned16(out_res)))
     return PSA_ERR_ALIGNMENT;
   const int N = s.H * s.W;
-  if (((long long)N * elem_bytes(s.dtype)) % 16 != 0) return PSA_ERR_ALIGNMENT;
   const int nh = s.num_heads, KD = s.key_dim;
-  if (s.dtype == PSA_DTYPE_F32) {
-    e = from_cuda(psa::launch_psa_fwd_f32((const float*)qkv, (float*)out, (float*)out_res, lse,
-                                          s.B, nh, KD, N, scale, st));
+  if (s.dtype == PSA_DTYPE_F32 || !tma_rows(s)) {
+    // fp32, or channel rows a tensor map cannot address: CUDA cores
+    psa::SimtArgs a = simt_nchw(qkv, s, scale);
+    a.out = out;
+    a.out_res = out_res;
+    a.lse = lse;
+    e = from_cuda(psa::launch_simt_fwd(a, true, s.dtype == PSA_DTYPE_BF16, KD, st));
   } else {
     CUtensorMap mqk, mv;
     const long long rows = (long long)s.B * nh * 4 * KD;
@@ -385,14 +421,28 @@ psa_status_t validate_bwd(const void* qkv, const void* dout, const float* lse, c
   psa_status_t e = check_shape(s);
   if (e != PSA_OK) return e;
   if (!isfinite(scale) || !(scale > 0.f)) return PSA_ERR_INVALID_ARG;
-  if (s.dtype != PSA_DTYPE_BF16) return PSA_ERR_UNSUPPORTED;
   if (s.key_dim != 32 && s.key_dim != 64) return PSA_ERR_UNSUPPORTED;
   if ((long long)s.B * s.num_heads > 65535) return PSA_ERR_UNSUPPORTED;
   if (!aligned16(qkv) || !aligned16(dout) || !aligned16(lse) || !aligned16(dqkv) ||
       !aligned16(delta) || (dvres && !aligned16(dvres)) || (out && !aligned16(out)))
     return PSA_ERR_ALIGNMENT;
-  if (((long long)s.H * s.W * 2) % 16 != 0) return PSA_ERR_ALIGNMENT;
   return PSA_OK;
+}
+
+// The backward on CUDA cores (fp32, or rows a tensor map cannot address).
+bool simt_bwd(const psa_shape_t& s) { return s.dtype == PSA_DTYPE_F32 || !tma_rows(s); }
+
+psa::SimtArgs simt_bwd_args(const void* qkv, const void* out, const void* dout, const float* lse,
+                            const void* dvres, void* dqkv, float* delta, const psa_shape_t& s,
+                            float scale) {
+  psa::SimtArgs a = simt_nchw(qkv, s, scale);
+  a.o = out;
+  a.dO = dout;
+  a.dvres = dvres;
+  a.dq = a.dk = a.dv = dqkv;
+  a.lse = const_cast<float*>(lse);
+  a.delta = delta;
+  return a;
 }
 
 // Tensor maps and kernel arguments of a validated fused backward call.
@@ -432,8 +482,12 @@ psa_status_t psa_attention_bwd_dq(const void* qkv, const void* out, const void* 
   CUtensorMap mqk, mv, mdo, mo;
   BwdArgs a;
   psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
-  if (e == PSA_OK)
-    e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &mo, &a);
+  if (e != PSA_OK) return e;
+  if (simt_bwd(s))
+    return from_cuda(psa::launch_simt_bwd_dq(
+        simt_bwd_args(qkv, out, dout, lse, nullptr, dqkv, delta, s, scale), true,
+        s.dtype == PSA_DTYPE_BF16, s.key_dim, st));
+  e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &mo, &a);
   if (e != PSA_OK) return e;
   return from_cuda(psa::launch_psa_bwd_dq(mqk, mv, mdo, mo, a, s.B * s.num_heads, s.key_dim, st));
 }
@@ -444,8 +498,12 @@ psa_status_t psa_attention_bwd_dkdv(const void* qkv, const void* dout, const flo
   CUtensorMap mqk, mv, mdo;
   BwdArgs a;
   psa_status_t e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
-  if (e == PSA_OK)
-    e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk, &mv, &mdo, nullptr, &a);
+  if (e != PSA_OK) return e;
+  if (simt_bwd(s))
+    return from_cuda(psa::launch_simt_bwd_dkdv(
+        simt_bwd_args(qkv, nullptr, dout, lse, dvres, dqkv, const_cast<float*>(delta), s, scale),
+        true, s.dtype == PSA_DTYPE_BF16, s.key_dim, st));
+  e = make_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, s, scale, &mqk, &mv, &mdo, nullptr, &a);
   if (e != PSA_OK) return e;
   return from_cuda(psa::launch_psa_bwd_dkdv(mqk, mv, mdo, a, s.B * s.num_heads, s.key_dim, st));
 }
@@ -463,6 +521,15 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
   BwdArgs a_dq, a_kv;
   e = validate_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, true, s, scale);
   if (e == PSA_OK) e = validate_bwd(qkv, dout, lse, dqkv, delta, dvres, nullptr, false, s, scale);
+  if (e != PSA_OK) return e;
+  if (simt_bwd(s)) {
+    // delta from the dQ kernel, in the workspace, then dK / dV
+    const psa::SimtArgs a = simt_bwd_args(qkv, out, dout, lse, dvres, dqkv, delta, s, scale);
+    const bool bf16 = s.dtype == PSA_DTYPE_BF16;
+    e = from_cuda(psa::launch_simt_bwd_dq(a, true, bf16, s.key_dim, st));
+    if (e != PSA_OK) return e;
+    return from_cuda(psa::launch_simt_bwd_dkdv(a, true, bf16, s.key_dim, st));
+  }
   if (e == PSA_OK)
     e = make_bwd(qkv, dout, lse, dqkv, delta, nullptr, out, s, scale, &mqk, &mv, &mdo, &mo, &a_dq);
   if (e == PSA_OK)

@@ -31,10 +31,22 @@ cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const FwdArgs& a, int KD, cudaStream_t st);
 
-cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
-                               float* lse, int BH, int N, int d, float scale, cudaStream_t st);
-cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* out_res, float* lse, int B,
-                               int nh, int KD, int N, float scale, cudaStream_t st);
+// CUDA-core path (attn_simt.cu): fp32 or bf16 storage, any N, fp32 arithmetic.
+// Raw layout: q, k, v, o, dO, dq, dk, dv are [BH, N, d] planes.  NCHW layout: q, k,
+// v point at the QKV tensor, dq, dk, dv at dQKV, o / dO / dvres / out / out_res
+// at [B, nh*2*KD, N] tensors.  Null outputs are skipped (out, out_res, lse).
+struct SimtArgs {
+  const void *q, *k, *v, *o, *dO, *dvres;
+  void *out, *out_res, *dq, *dk, *dv;
+  float* lse;    // forward: written (nullable); backward: read
+  float* delta;  // [BH, N]: written by the dQ kernel, read by the dK/dV kernel
+  int N, BH, nh, qkv_ch, out_ch;
+  float scale;
+};
+cudaError_t launch_simt_fwd(const SimtArgs& a, bool nchw, bool bf16, int dqk, cudaStream_t st);
+cudaError_t launch_simt_bwd_dq(const SimtArgs& a, bool nchw, bool bf16, int dqk, cudaStream_t st);
+cudaError_t launch_simt_bwd_dkdv(const SimtArgs& a, bool nchw, bool bf16, int dqk,
+                                 cudaStream_t st);
 
 // Launches kern with programmatic stream serialization: its CTAs may become
 // resident and run their prologue (barrier set-up, tensor memory allocation)

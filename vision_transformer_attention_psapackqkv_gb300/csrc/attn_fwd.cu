@@ -40,8 +40,8 @@
 // DV = 2*KD), PsaMergeAttn, and optionally PsaExtractV (the slot whose query tile
 // index equals the key tile index copies that V tile out of shared memory).
 //
-// fp32 path (CUDA cores): the same online softmax with one thread per query
-// row and fp32 arithmetic throughout (a 1e-4 bound rules out tf32 inputs).
+// fp32 storage and maps whose rows TMA cannot address run on CUDA cores
+// (attn_simt.cu).
 #include <math.h>
 
 #include <algorithm>
@@ -640,83 +640,6 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
   }
 }
 
-// ------------------------------------------------------------------ fp32 path
-template <int DQK, int DV, bool kNCHW>
-__global__ void __launch_bounds__(128)
-    attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                        const float* __restrict__ v, float* __restrict__ out,
-                        float* __restrict__ out_res, float* __restrict__ lse, int N, int nh,
-                        int qkv_ch, int out_ch, float scale) {
-  constexpr int TK = 32;
-  __shared__ float sk[TK][DQK];
-  __shared__ float sv[TK][DV];
-  const int bh = blockIdx.y;
-  const int i = blockIdx.x * 128 + threadIdx.x;
-  const int b = bh / nh, hd = bh % nh;
-  // element (row n, column d) of the Q / K / V operand of this head
-  auto at = [&](const float* base, int plane, int n, int d, int width) -> float {
-    if (kNCHW)
-      return base[((long long)b * qkv_ch + hd * 4 * DQK + plane * DQK + d) * N + n];
-    return base[((long long)bh * N + n) * width + d];
-  };
-  float qr[DQK];
-#pragma unroll
-  for (int d = 0; d < DQK; ++d) qr[d] = (i < N) ? at(q, 0, i, d, DQK) : 0.f;
-  float acc[DV];
-#pragma unroll
-  for (int c = 0; c < DV; ++c) acc[c] = 0.f;
-  float m = -INFINITY, l = 0.f;
-  for (int kv0 = 0; kv0 < N; kv0 += TK) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < TK * DQK; e += 128) {
-      const int jj = e / DQK, d = e % DQK;
-      sk[jj][d] = (kv0 + jj < N) ? at(k, 1, kv0 + jj, d, DQK) : 0.f;
-    }
-    for (int e = threadIdx.x; e < TK * DV; e += 128) {
-      const int jj = e / DV, c = e % DV;
-      sv[jj][c] = (kv0 + jj < N) ? at(v, 2, kv0 + jj, c, DV) : 0.f;
-    }
-    __syncthreads();
-    const int nv = min(TK, N - kv0);
-    float s[TK];
-    float mx = m;
-#pragma unroll
-    for (int jj = 0; jj < TK; ++jj) {
-      float dot = 0.f;
-#pragma unroll
-      for (int d = 0; d < DQK; ++d) dot = fmaf(qr[d], sk[jj][d], dot);
-      s[jj] = (jj < nv) ? dot * scale : -INFINITY;
-      mx = fmaxf(mx, s[jj]);
-    }
-    const float corr = expf(m - mx);  // m = -inf on the first tile gives 0
-    l *= corr;
-#pragma unroll
-    for (int c = 0; c < DV; ++c) acc[c] *= corr;
-    m = mx;
-#pragma unroll
-    for (int jj = 0; jj < TK; ++jj) {
-      const float p = expf(s[jj] - m);
-      l += p;
-#pragma unroll
-      for (int c = 0; c < DV; ++c) acc[c] = fmaf(p, sv[jj][c], acc[c]);
-    }
-  }
-  if (i >= N) return;
-  const float inv_l = 1.f / l;
-  for (int c = 0; c < DV; ++c) {
-    if (kNCHW) {
-      const long long o = ((long long)b * out_ch + hd * DV + c) * N + i;
-      if (out) out[o] = acc[c] * inv_l;
-      if (out_res) out_res[o] = acc[c] * inv_l + at(v, 2, i, c, DV);  // Out + V
-    } else {
-      out[((long long)bh * N + i) * DV + c] = acc[c] * inv_l;
-    }
-  }
-  if (lse) lse[(long long)bh * N + i] = m + logf(l);
-}
-
-
-
 template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
 cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUtensorMap& mV,
                       const FwdArgs& a, cudaStream_t st) {
@@ -731,17 +654,6 @@ cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUten
   return launch_pdl(kern, dim3((unsigned)ctas), dim3(C::kThreads), C::SMEM_BYTES, st, mQK, mK,
                     mV, a);
 }
-
-template <int DQK, int DV, bool kNCHW>
-cudaError_t launch_f32(const float* q, const float* k, const float* v, float* out,
-                       float* out_res, float* lse, int BH, int N, int nh, int qkv_ch, int out_ch,
-                       float scale, cudaStream_t st) {
-  dim3 grid((N + 127) / 128, BH);
-  attn_fwd_f32_kernel<DQK, DV, kNCHW><<<grid, 128, 0, st>>>(q, k, v, out, out_res, lse, N, nh,
-                                                          qkv_ch, out_ch, scale);
-  return cudaGetLastError();
-}
-
 
 }  // namespace
 
@@ -764,22 +676,6 @@ cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
   if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4, false>(mQK, mQK, mV, a, st);
   // DV = 128: two accumulators would not leave room for a second CTA's tensor memory
   return launch_tc<64, 128, true, 1, 1, 2, false>(mQK, mQK, mV, a, st);
-}
-
-cudaError_t launch_fa2_fwd_f32(const float* q, const float* k, const float* v, float* o,
-                               float* lse, int BH, int N, int d, float scale, cudaStream_t st) {
-  if (d == 32) return launch_f32<32, 32, false>(q, k, v, o, nullptr, lse, BH, N, 1, 0, 0, scale, st);
-  return launch_f32<64, 64, false>(q, k, v, o, nullptr, lse, BH, N, 1, 0, 0, scale, st);
-}
-
-cudaError_t launch_psa_fwd_f32(const float* qkv, float* out, float* out_res, float* lse, int B,
-                               int nh, int KD, int N, float scale, cudaStream_t st) {
-  const int BH = B * nh;
-  if (KD == 32)
-    return launch_f32<32, 64, true>(qkv, qkv, qkv, out, out_res, lse, BH, N, nh, nh * 4 * KD,
-                                    nh * 2 * KD, scale, st);
-  return launch_f32<64, 128, true>(qkv, qkv, qkv, out, out_res, lse, BH, N, nh, nh * 4 * KD,
-                                   nh * 2 * KD, scale, st);
 }
 
 }  // namespace psa
