@@ -60,6 +60,7 @@ def _load():
         lib.oracle_psa_fwd.argtypes = [P, P, P, P, I, I, I, I, D, I]
         lib.oracle_psa_bwd.argtypes = [P, P, P, P, I, I, I, I, D, I]
         lib.oracle_psa_fwd_residual.argtypes = [P, P, P, I, I, I, I, D, I]
+        lib.oracle_qkv_conv.argtypes = [P, P, P, P, I, I, I, I]
         _lib = lib
     return _lib
 
@@ -204,6 +205,20 @@ def psa_fwd(qkv, num_heads: int, key_dim: int, scale: float, nthreads: int | Non
     _load().oracle_psa_fwd(_ptr(qkv), _ptr(out), _ptr(lse), _ptr(vres), B, num_heads, key_dim,
                            H * W, float(scale), nthreads or default_threads())
     return out, lse, vres
+
+
+def qkv_conv(x, w, bias=None):
+    """QKV 1x1 convolution (float64): x [B, cin, H, W], w [cout, cin], bias [cout] or
+    None -> [B, cout, H, W]."""
+    x = _c(x, np.float64)
+    w = _c(w, np.float64)
+    bias = None if bias is None else _c(bias, np.float64)
+    B, cin, H, W = x.shape
+    cout = w.shape[0]
+    assert w.shape == (cout, cin)
+    out = np.empty((B, cout, H, W))
+    _load().oracle_qkv_conv(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, cin, cout, H * W)
+    return out
 
 
 def psa_fwd_residual(qkv, num_heads: int, key_dim: int, scale: float, nthreads: int | None = None):

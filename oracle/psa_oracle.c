@@ -436,6 +436,24 @@ void oracle_psa_fwd(const double *qkv, double *out, double *lse, double *vres, i
 
 /* Backward of the chain above: dqkv = d(sum(dout o out) + sum(dvres o vres)) / dqkv,
  * obtained by running each step's adjoint in reverse order (dvres may be NULL). */
+/* The QKV 1x1 convolution whose NCHW output PsaPackQkv repacks (page "Custom
+ * Kernels", section "Position-Sensitive Attention (PSA)": PsaPackQkv takes a QKV
+ * conv's NCHW output): qkv[b, o, n] = bias[o] + sum_c w[o, c] x[b, c, n], with
+ * x [B, cin, N], w [cout, cin] and bias [cout] (NULL: no bias).  The plain
+ * definition, one output element at a time. */
+void oracle_qkv_conv(const double *x, const double *w, const double *bias, double *qkv, int B,
+                     int cin, int cout, int N)
+{
+    for (long b = 0; b < B; ++b)
+        for (long o = 0; o < cout; ++o)
+            for (long n = 0; n < N; ++n) {
+                double acc = bias ? bias[o] : 0.0;
+                for (long c = 0; c < cin; ++c)
+                    acc += w[o * cin + c] * x[(b * cin + c) * N + n];
+                qkv[(b * cout + o) * N + n] = acc;
+            }
+}
+
 /* The attention output with its residual path added: out_res = out + vres, where
  * out is the merged attention output and vres the PsaExtractV output of
  * oracle_psa_fwd (page "Custom Kernels", section "Position-Sensitive Attention
