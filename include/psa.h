@@ -66,6 +66,20 @@ typedef struct {
     psa_dtype_t dtype;
 } psa_shape_t;
 
+/* ---- QKV convolution ---------------------------------------------------------- */
+
+/* The QKV 1x1 convolution whose NCHW output PsaPackQkv and the fused PSA forward
+ * read ("Custom Kernels", section "Position-Sensitive Attention (PSA)": PsaPackQkv
+ * takes a QKV conv's NCHW output): qkv[b, o, n] = bias[o] + sum_c w[o, c] x[b, c, n]
+ * for x_nchw [B, cin, H, W], weight [cout, cin] (row-major), bias [cout] fp32
+ * (NULL: none) and qkv_nchw [B, cout, H, W]; bf16 storage, fp32 accumulation,
+ * outputs rounded once.  On the tensor cores when cin and H*W are multiples of 8,
+ * on CUDA cores otherwise.  Pointers 16-byte aligned (bias 4-byte);
+ * PSA_ERR_INVALID_ARG for a NULL required pointer or a non-positive size. */
+psa_status_t psa_qkv_conv(const void *x_nchw, const void *weight, const float *bias,
+                          void *qkv_nchw, int B, int cin, int cout, int H, int W,
+                          cudaStream_t stream);
+
 /* ---- layout kernels (bit-exact element copies) ------------------------------ */
 
 /* PsaPackQkv ("Custom Kernels", section "Position-Sensitive Attention (PSA)"):

@@ -148,3 +148,14 @@ def test_residual_forward_validation(lib):
     assert f(A, MIS, None, None, _shape(), 0.17, None) == ALIGNMENT
     assert f(A, A, MIS, None, _shape(), 0.17, None) == ALIGNMENT
     assert f(A, A, None, None, _shape(KD=16), 0.17, None) == UNSUPPORTED
+
+
+@placeholder_only
+def test_qkv_conv_validation(lib):
+    f = lib.psa_qkv_conv
+    assert f(None, A, None, A, 1, 8, 8, 4, 4, None) == INVALID
+    assert f(A, A, None, None, 1, 8, 8, 4, 4, None) == INVALID
+    assert f(A, A, None, A, 0, 8, 8, 4, 4, None) == INVALID
+    assert f(A, A, None, A, 1, 8, -8, 4, 4, None) == INVALID
+    assert f(MIS, A, None, A, 1, 8, 8, 4, 4, None) == ALIGNMENT
+    assert f(A, A, P(0x10002), A, 1, 8, 8, 4, 4, None) == ALIGNMENT   # bias not 4-byte aligned

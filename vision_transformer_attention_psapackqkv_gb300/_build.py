@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpsa_gb300.so")
 SOURCES = ["api.cu", "layout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_fused.cu", "attn_simt.cu",
-           "noalloc.cu"]
+           "qkv_conv.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "attn.cuh", "layout.cuh", "tiles.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC",

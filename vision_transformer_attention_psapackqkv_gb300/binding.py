@@ -32,7 +32,7 @@ class PsaShape(ctypes.Structure):
 
 
 EXPORTED = (
-    "psa_pack_qkv", "psa_unpack_qkv", "psa_extract_v", "psa_merge_attn", "psa_unmerge_attn",
+    "psa_qkv_conv", "psa_pack_qkv", "psa_unpack_qkv", "psa_extract_v", "psa_merge_attn", "psa_unmerge_attn",
     "flash_attn2_fwd", "flash_attn2_bwd_dq", "flash_attn2_bwd_dkdv", "psa_attention_fwd",
     "psa_attention_fwd_residual", "psa_attention_bwd", "psa_attention_bwd_dq", "psa_attention_bwd_dkdv", "psa_attention_bwd_noalloc",
     "psa_attention_bwd_workspace_size", "psa_status_string",
@@ -55,6 +55,7 @@ def load(path: str | None = None):
     lib = ctypes.CDLL(path)
     P, I, F, S, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, PsaShape, ctypes.c_size_t
     sigs = {
+        "psa_qkv_conv": [P, P, P, P, I, I, I, I, I, P],
         "psa_pack_qkv": [P, P, S, P],
         "psa_unpack_qkv": [P, P, S, P],
         "psa_extract_v": [P, P, S, P],
@@ -116,6 +117,15 @@ def shape_of(qkv, num_heads: int, key_dim: int) -> PsaShape:
     if C != num_heads * 4 * key_dim:
         raise ValueError(f"QKV has {C} channels, expected num_heads*4*key_dim = {num_heads * 4 * key_dim}")
     return PsaShape(B, num_heads, key_dim, H, W, dtype_code(qkv))
+
+
+# ------------------------------------------------------------------ QKV convolution
+def psa_qkv_conv(x, weight, bias, qkv, stream=None):
+    """x [B, cin, H, W] bf16, weight [cout, cin] bf16, bias [cout] fp32 or None -> qkv."""
+    Bn, cin, H, W = x.shape
+    cout = weight.shape[0]
+    _check("psa_qkv_conv", load().psa_qkv_conv(_ptr(x), _ptr(weight), _ptr(bias), _ptr(qkv), Bn, cin,
+                                                cout, H, W, _stream(stream)))
 
 
 # ------------------------------------------------------------------ layout

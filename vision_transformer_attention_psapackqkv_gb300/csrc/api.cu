@@ -137,6 +137,29 @@ bool map_nchw(CUtensorMap* m, const void* base, long long rows, int N, int box_r
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the QKV convolution: w [cout, cin] (box {64, 128}) and x viewed as
+// 3-D (N, cin, B) (box {64, 64, 1}); positions and channels past the ends read as 0.
+bool map_conv(CUtensorMap* mw, CUtensorMap* mx, const void* w, const void* x, int B, int cin,
+              int cout, int N) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t wd[2] = {(cuuint64_t)cin, (cuuint64_t)cout};
+  cuuint64_t ws[1] = {(cuuint64_t)cin * 2};
+  cuuint32_t wb[2] = {64, 128};
+  cuuint32_t e2[2] = {1, 1};
+  if (enc(mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), wd, ws, wb, e2,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cuuint64_t xd[3] = {(cuuint64_t)N, (cuuint64_t)cin, (cuuint64_t)B};
+  cuuint64_t xs[2] = {(cuuint64_t)N * 2, (cuuint64_t)cin * N * 2};
+  cuuint32_t xb[3] = {64, 64, 1};
+  cuuint32_t e3[3] = {1, 1, 1};
+  return enc(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), xd, xs, xb, e3,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 psa_status_t check_fa2(const void* const* ptrs, int nptr, int BH, int n_ctx, int head_dim,
                        float scale, psa_dtype_t dtype) {
   for (int i = 0; i < nptr; ++i) {
@@ -171,6 +194,32 @@ psa_status_t psa_debug_wait_timeout(unsigned long long limit_ns, cudaStream_t st
   if (limit_ns == 0 || limit_ns > 100000000ull) return PSA_ERR_INVALID_ARG;
   psa::wait_timeout_probe_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_ns);
   return from_cuda(cudaGetLastError());
+}
+
+psa_status_t psa_qkv_conv(const void* x, const void* w, const float* bias, void* qkv, int B,
+                          int cin, int cout, int H, int W, cudaStream_t st) {
+  if (!x || !w || !qkv) return PSA_ERR_INVALID_ARG;
+  if (B <= 0 || cin <= 0 || cout <= 0 || H <= 0 || W <= 0) return PSA_ERR_INVALID_ARG;
+  const long long N = (long long)H * W;
+  if (N > (1LL << 30) || (long long)B * cin * N > (1LL << 40) || (long long)B * cout * N > (1LL << 40) ||
+      (long long)B * cout > (1LL << 30) || (long long)B * cin > (1LL << 30))
+    return PSA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(qkv) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3)))
+    return PSA_ERR_ALIGNMENT;
+  psa::ConvArgs a{};
+  a.B = B;
+  a.cin = cin;
+  a.cout = cout;
+  a.N = (int)N;
+  a.bias = bias;
+  a.out = static_cast<__nv_bfloat16*>(qkv);
+  if (cin % 8 == 0 && N % 8 == 0) {
+    CUtensorMap mw, mx;
+    if (!map_conv(&mw, &mx, w, x, B, cin, cout, (int)N)) return PSA_ERR_CUDA;
+    return from_cuda(psa::launch_qkv_conv_tc(mw, mx, a, st));
+  }
+  if (cout > 65535 || B > 65535) return PSA_ERR_UNSUPPORTED;
+  return from_cuda(psa::launch_qkv_conv_simt(x, w, a, st));
 }
 
 psa_status_t psa_get_last_device_error(cudaStream_t stream) {

@@ -118,4 +118,18 @@ cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
                                  const CUtensorMap& mDO, const BwdArgs& a, int KD,
                                  cudaStream_t st);
 
+// QKV 1x1 convolution (qkv_conv.cu): out [B, cout, N] = w [cout, cin] . x [B, cin, N]
+// + bias [cout] (nullable, fp32), bf16 storage, fp32 accumulation.
+struct ConvArgs {
+  int B, cin, cout, N;
+  const float* bias;
+  __nv_bfloat16* out;
+};
+// Tensor cores: mW 2-D over w (box {64, 128}), mX 3-D over x (box {64, 64, 1}),
+// both with the 128-byte swizzle; needs cin % 8 == 0 and N % 8 == 0.
+cudaError_t launch_qkv_conv_tc(const CUtensorMap& mW, const CUtensorMap& mX, const ConvArgs& a,
+                               cudaStream_t st);
+// CUDA cores, any shape.
+cudaError_t launch_qkv_conv_simt(const void* x, const void* w, const ConvArgs& a, cudaStream_t st);
+
 }  // namespace psa

@@ -196,3 +196,13 @@ def rescale_psa_inputs(B: int, num_heads: int, key_dim: int, H: int, W: int, see
     out = {"qkv": f32_to_bf16(qkv.reshape(B, C, H, W).astype(np.float32))}
     out["dout"] = f32_to_bf16(normal_f32((B, num_heads * 2 * KD, H, W), seed, 1.0, 1))
     return out
+
+
+def conv_inputs(B: int, cin: int, cout: int, H: int, W: int, seed: int, with_bias: bool = True):
+    """Input feature map x [B, cin, H, W] (N(0, 1)), QKV weights w [cout, cin]
+    (N(0, 1) / sqrt(cin), so outputs have unit scale) as bf16 bits, and bias [cout]
+    (N(0, 0.25), float32) or None.  Synthetic weights: no trained model is involved."""
+    x = f32_to_bf16(normal_f32((B, cin, H, W), seed, 1.0, 10))
+    w = f32_to_bf16(normal_f32((cout, cin), seed, 1.0 / float(np.sqrt(cin)), 11))
+    bias = normal_f32((cout,), seed, 0.5, 12) if with_bias else None
+    return {"x": x, "w": w, "bias": bias}
