@@ -44,11 +44,34 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "psa_fwdbwd_n400"
 METRIC = "PSA attention fwd+bwd tokens/s and TFLOP/s at N=400, KEY_DIM=32; % roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per call of each step part, measured with ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum) on this workload for the current
-# kernels; to be re-measured whenever a kernel changes.
-MEASURED_TRAFFIC = {"fwd": 26.26e6 + 0.006e6, "bwd": 52.90e6 + 1.51e6,
-                    "bwd_dq": 52.88e6 + 0.33e6, "bwd_dkdv": 40.21e6 + 0.30e6}
+# DRAM bytes per call of each step part come from the ncu capture recorded in
+# profiles/dram_traffic.json, which also records a hash of the kernel source the
+# capture ran; a part whose source has changed since reports no traffic.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "vision_transformer_attention_psapackqkv_gb300", "csrc")
+
+
+def source_hash(files):
+    """sha256 (first 16 hex digits) over the named kernel source files."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(part):
+    """(bytes, note) of the recorded ncu capture of `part`, or (None, reason)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["parts"][part]
+    except (OSError, KeyError, ValueError):
+        return None, "no capture recorded"
+    if source_hash(rec["sources"]) != rec["source_hash"]:
+        return None, "kernel changed since the capture of " + rec["captured"]
+    return rec["dram_bytes"], rec["kernel"] + ", ncu capture of " + rec["captured"]
 
 
 def load_peaks():
@@ -391,7 +414,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": km["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = MEASURED_TRAFFIC.get(dom)
+    roof["traffic"], roof["traffic_source"] = measured_traffic(dom)
     roof["kernel"] = dom
     roof["peak_source"] = peak_src
     step_roof_time = max(step_model["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
@@ -411,6 +434,10 @@ def run_ours(args, rank, world, local_rank):
                           "flops": step_model["flops"], "bytes": step_model["bytes"],
                           "peak_source": peak_src},
         "kernel_us": {k: v * 1e3 for k, v in per.items()},
+        # consecutive kernels overlap their prologue with the previous kernel's tail
+        # (programmatic dependent launch), so the parts, timed with events between
+        # them, add up to more than ms_per_step
+        "pdl": True,
         "roofline": roof,
         "e2e": {"value": job_throughput(tokens_per_step, world, Ke, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
@@ -478,6 +505,27 @@ def _time_loop(torch, fn, iters, warmup):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters * 1e-3  # seconds per call
+
+
+def _time_graph(torch, fn, iters, warmup):
+    """Seconds per call of fn(i), i = 0 .. iters-1, replayed from a CUDA graph so the
+    host's launch rate does not set the pace of short kernels."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(iters):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters * 1e-3
 
 
 def run_sweep(args):
@@ -601,6 +649,8 @@ def run_layout(args):
     peaks, src = load_peaks()
     hbm = peaks["hbm_gbs"]
     w = PSA_WORKLOADS[WORKLOAD]
+    # every case is replayed from a CUDA graph of `iters` calls (short kernels would
+    # otherwise wait on the host's launches)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(w.seed)
     rnd = lambda *shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
@@ -637,12 +687,12 @@ def run_layout(args):
         ("psa_extract_v", 2 * half_b, lambda s: B.psa_extract_v(s["qkv"], s["v"], shape)),
     ]
     lines = []
-    iters = 200
+    iters = args.iters
     for name, nbytes, fn in cases:
         for l2 in ("cold", "hot"):
             use = sets if l2 == "cold" else sets[:1]
             with ClockSampler() as clk:
-                sec = _time_loop(torch, lambda i: fn(use[i % len(use)]), iters, 2 * len(use))
+                sec = _time_graph(torch, lambda i: fn(use[i % len(use)]), iters, min(2 * len(use), iters))
             gbs = nbytes / sec / 1e9
             line = {"metric": "layout kernel GB/s (algorithmic bytes)", "workload": WORKLOAD,
                     "kernel": name, "l2": l2, "value": gbs, "unit": "GB/s", "us": sec * 1e6,
@@ -675,6 +725,34 @@ def run_layout(args):
     def bwd_fused(s):
         B.psa_attention_bwd(s["qkv"], s["out"], s["dout"], s["lse"], None, s["dqkv"], s["ws"], shape, scale)
 
+    # the QKV 1x1 convolution of this block (c = nh*2*KD input channels -> nh*4*KD)
+    gw = torch.Generator(device="cuda")
+    gw.manual_seed(w.seed + 100)
+    cin, cout = w.out_channels, w.qkv_channels
+    conv_sets = [{"x": torch.randn((w.B, cin, w.H, w.W), generator=gw, device="cuda").to(torch.bfloat16),
+                  "qkv": s["qkv"], "out": s["out"]} for s in sets]
+    wt = (torch.randn((cout, cin), generator=gw, device="cuda") / math.sqrt(cin)).to(torch.bfloat16)
+    bias = torch.randn((cout,), generator=gw, device="cuda") * 0.5
+    conv_flops = 2.0 * w.B * cout * cin * N
+    conv_bytes = (w.B * cin * N + cout * cin + w.B * cout * N) * 2 + cout * 4
+    for name, fn, flops, nbytes in (
+            ("psa_qkv_conv", lambda c: B.psa_qkv_conv(c["x"], wt, bias, c["qkv"]), conv_flops, conv_bytes),
+            ("psa_qkv_conv -> psa_attention_fwd",
+             lambda c: (B.psa_qkv_conv(c["x"], wt, bias, c["qkv"]),
+                        B.psa_attention_fwd(c["qkv"], c["out"], None, None, shape, scale)),
+             conv_flops + work_model(w)[0]["fwd"]["flops"], None)):
+        with ClockSampler() as clk:
+            sec = _time_graph(torch, lambda i: fn(conv_sets[i % nsets]), iters, min(2 * nsets, iters))
+        line = {"metric": "QKV 1x1 conv (tensor cores)", "workload": WORKLOAD, "path": name,
+                "config": {"B": w.B, "cin": cin, "cout": cout, "H": w.H, "W": w.W},
+                "us": sec * 1e6, "tflops": flops / sec / 1e12, "l2": "cold", "clocks": clk.summary()}
+        if nbytes:
+            line["hbm"] = {"algorithmic_bytes": nbytes, "gbs": nbytes / sec / 1e9,
+                           "frac": nbytes / sec / 1e9 / hbm, "peak_source": src}
+            line["tensor"] = {"frac": flops / sec / 1e12 / peaks["bf16_tflops"], "peak_source": src}
+        lines.append(line)
+        print(json.dumps(line), flush=True)
+
     for st in sets:
         fwd_chain(st)
     kmodel, _ = work_model(w)
@@ -683,7 +761,7 @@ def run_layout(args):
                                ("unfused backward chain (without the dQ / dK half sums)", bwd_chain, 6, "bwd"),
                                ("psa_attention_bwd", bwd_fused, 1, "bwd")):
         with ClockSampler() as clk:
-            sec = _time_loop(torch, lambda i: fn(sets[i % nsets]), iters, 2 * nsets)
+            sec = _time_graph(torch, lambda i: fn(sets[i % nsets]), iters, min(2 * nsets, iters))
         km = kmodel[part]
         line = {"metric": "PSA attention step part, unfused chain vs fused", "workload": WORKLOAD,
                 "path": name, "launches": nk, "us": sec * 1e6, "l2": "cold",
@@ -748,7 +826,8 @@ def main():
     ap.add_argument("--split-bwd", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--layout", action="store_true",
-                    help="time the data-movement kernels and the unfused chain instead")
+                    help="time the data-movement kernels, the QKV conv and the unfused chain instead")
+    ap.add_argument("--iters", type=int, default=200, help="with --layout: timed calls per case")
     ap.add_argument("--case", default=None,
                     help="with --sweep: run only the case of this name (e.g. fa2_bh64_n4096_d64)")
     args = ap.parse_args()
