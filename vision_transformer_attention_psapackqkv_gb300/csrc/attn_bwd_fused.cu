@@ -20,29 +20,36 @@
 // PsaMergeAttn and PsaPackQkv are folded into the tile addressing, the optional
 // PsaExtractV gradient is added into the V channels), as in the split kernels.
 //
-// Fused kernel: one CTA per SM (persistent over heads), 768 threads.  A step is
+// Fused kernel: one CTA per SM (persistent over heads), 896 threads.  A step is
 // (key tile kt of 128 keys, query sub-tile j of 64 queries); dQ is accumulated
 // per 128-query tile, i.e. once every two steps.
 //   warps 0-15 row threads: warp w serves TMEM lanes 32(w%4).. (key rows) and
 //              query columns 16(w/4)..+15 of the step (four warps per SM
 //              sub-partition, so one warp's waits overlap the others'
-//              exponentials); they turn S^T / dP^T into bf16 P^T and dS^T in
-//              shared memory, and compute each head's delta at its start;
+//              exponentials); they turn S^T / dP^T into bf16 P^T and dS^T, which
+//              they write into their own TMEM lanes (for dV and dK) and dS^T also
+//              into shared memory (for dQ, which needs it transposed), and
+//              compute each head's delta at its start;
 //   warp 16    TMA producer (K / V per key tile, double-buffered; Q / dO per step
 //              in a ring; lse2 of a head into shared memory, from registers
 //              loaded one head ahead);
-//   warp 17    issues S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffers
-//              (64 + 64 columns each, by step parity) and owns the 512 columns;
-//   warp 18    issues the gradient products into dV (64 columns), dK (32) and
-//              dQ of up to 4 query tiles (4 x 32);
-//   warp 19    idle;
-//   warps 20-23 epilogue: read dV / dK of a finished key tile out of tensor
+//   warps 17-21 issue the products, one thread each: S^T = K Q^T and dP^T =
+//              V dO^T into TMEM (64 + 64 columns) as soon as the row threads
+//              hold the previous step's in registers (warp 17 also owns the 512
+//              columns); dV += P^T dO and dK += dS^T Q (P^T, dS^T read as the A
+//              operand from tensor memory); dQ of up to 4 query tiles (4 x 32);
+//   warps 22-23 idle;
+//   warps 24-27 epilogue: read dV / dK of a finished key tile out of tensor
 //              memory, hand the accumulators back, and write them to dQKV (with
 //              dVres); read and write dQ once a head is done.
-// With two S^T / dP^T buffers the products of step s+1 run while the row
-// threads work on step s; P^T is double-buffered and dS^T pair-buffered in
-// shared memory, so neither side waits for the other's previous step.  Two
-// issuing threads keep the tensor pipe fed while one of them waits.  The row
+// The products of step s+1 run while the row threads work on step s; P^T and
+// dS^T are double-buffered in tensor memory and dS^T pair-buffered in shared
+// memory, so neither side waits for the other's previous step.  Five issuing
+// threads keep the tensor pipe fed (one thread alone issues one MMA per ~130
+// cycles).  Keeping P^T and
+// dS^T out of shared memory for dV and dK halves the shared-memory traffic of a
+// step, which the MMAs' operand reads, the row threads' stores and the TMA
+// fills otherwise share.  The row
 // threads never wait for a key tile's products to drain: the epilogue warps do,
 // while the rows already work on the next key tile's first steps.
 //   dV += P^T dO,  dK += dS^T Q  (per step);  dQ_t += dS K  (dS read as the
@@ -91,10 +98,11 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[NC], const uint3
 template <int DQK, int DV, int ST>
 struct FusedCfg {
   static constexpr int BK = 128, BQ = 64, QT = 128, MAXN = kFusedBwdMaxN, MAXQT = MAXN / QT;
-  static constexpr int kRowWarps = 16, kThreads = 32 * kRowWarps + 256;
-  static constexpr int kProducer = kRowWarps, kSIssuer = kRowWarps + 1, kGIssuer = kRowWarps + 2;
-  // four epilogue warps, warp % 4 = TMEM lane quadrant
-  static constexpr int kEpiWarp0 = kRowWarps + 4, kEpiThreads = 128;
+  static constexpr int kRowWarps = 16, kThreads = 32 * kRowWarps + 384;
+  // producer, then the issuers of S^T (TMEM owner), dP^T, dV, dK and dQ, two idle
+  // warps, then four epilogue warps (warp % 4 = TMEM lane quadrant)
+  static constexpr int kProducer = kRowWarps, kIssS = kRowWarps + 1, kIssLast = kIssS + 4;
+  static constexpr int kEpiWarp0 = kRowWarps + 8, kEpiThreads = 128;
   static constexpr uint32_t K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
   static constexpr uint32_t Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
   static constexpr uint32_t STAGE_BYTES = Q_BYTES + DO_BYTES;
@@ -103,14 +111,15 @@ struct FusedCfg {
   static constexpr uint32_t HSTAT_BYTES = 2 * MAXN * 4;  // -lse2[MAXN], -delta[MAXN] of a head
   static constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + 2 * K_BYTES;
   static constexpr uint32_t OFF_STAGE = OFF_V + 2 * V_BYTES;
-  static constexpr uint32_t OFF_PT = OFF_STAGE + ST * STAGE_BYTES;  // P^T: two buffers
-  static constexpr uint32_t OFF_DST = OFF_PT + 2 * HALF_BYTES;      // dS^T: two pair buffers
+  static constexpr uint32_t OFF_DST = OFF_STAGE + ST * STAGE_BYTES;  // dS^T: two pair buffers
   static constexpr uint32_t OFF_HSTAT = OFF_DST + 2 * PAIR_BYTES;  // two heads
   static constexpr uint32_t OFF_DSCR = OFF_HSTAT + 2 * HSTAT_BYTES;  // delta partial sums
   static constexpr uint32_t OFF_BAR = OFF_DSCR + 8 * MAXN * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
-  // TMEM columns: S^T_b at 64 b, dP^T_b at 128 + 64 b
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = TM_DV + DV;
+  // TMEM columns: S^T, dP^T (fp32), then P^T_b and dS^T_b (bf16 pairs, 32 columns
+  // per 64 queries, b = step parity), dV, dK, dQ of up to 4 query tiles
+  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_PT = 128, TM_DST = 192;
+  static constexpr uint32_t TM_DV = 256, TM_DK = TM_DV + DV;
   static constexpr uint32_t TM_DQ = TM_DK + DQK;
   static_assert(TM_DQ + MAXQT * DQK <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024 && SMEM_BYTES > 114 * 1024, "one CTA per SM");
@@ -120,8 +129,8 @@ struct FusedCfg {
 
 struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[8], q_empty[8];
-  uint64_t s_full[2], s_free[2], p_full[2], g_done[2], hs_full[2], hs_free[2];
-  uint64_t acc_full, acc_free, dq_full, dq_free, mma_done[2];
+  uint64_t s_full, s_free, p_full[2], g_done[2], hs_full[2], hs_free[2];
+  uint64_t acc_full, acc_free, dq_full, dq_free, mma_done[5];
   uint64_t dl_part, dl_full;  // a head's delta: partial sums written, delta written
 };
 static_assert(sizeof(FusedBars) + 8 <= 512, "barrier area");
@@ -134,7 +143,7 @@ __device__ __forceinline__ uint64_t off_ch_by_pos(int kk) {
 }
 
 template <int DQK, int DV, int ST>
-__global__ void __launch_bounds__(768, 1)
+__global__ void __launch_bounds__(896, 1)
     attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -161,22 +170,26 @@ __global__ void __launch_bounds__(768, 1)
   auto out_row = [&](int bh) { return (bh / args.nh) * args.out_ch + (bh % args.nh) * DV; };
 
   if (threadIdx.x == 0) {
+    // arrival counts: K / V are read by the S^T, dP^T and dQ issuers, a Q / dO
+    // stage by the S^T, dP^T, dV and dK issuers; S^T / dP^T come from two
+    // issuers, P^T / dS^T are read by the dV, dK and dQ issuers, and the dV / dK
+    // accumulators are filled by two
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.kv_full[i], 1);
-      mbar_init(&b.kv_empty[i], 1);
-      mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.s_free[i], 32 * C::kRowWarps);
+      mbar_init(&b.kv_empty[i], 3);
       mbar_init(&b.p_full[i], 32 * C::kRowWarps);
-      mbar_init(&b.g_done[i], 1);
+      mbar_init(&b.g_done[i], 3);
       mbar_init(&b.hs_full[i], 32);
       mbar_init(&b.hs_free[i], 32 * C::kRowWarps);
-      mbar_init(&b.mma_done[i], 1);
     }
+    for (int i = 0; i < 5; ++i) mbar_init(&b.mma_done[i], 1);
+    mbar_init(&b.s_full, 2);
+    mbar_init(&b.s_free, 32 * C::kRowWarps);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&b.q_full[i], 1);
-      mbar_init(&b.q_empty[i], 1);
+      mbar_init(&b.q_empty[i], 4);
     }
-    mbar_init(&b.acc_full, 1);
+    mbar_init(&b.acc_full, 2);
     mbar_init(&b.acc_free, C::kEpiThreads);
     mbar_init(&b.dq_full, 1);
     mbar_init(&b.dq_free, C::kEpiThreads);
@@ -185,7 +198,7 @@ __global__ void __launch_bounds__(768, 1)
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == C::kSIssuer) {
+  if (warp == C::kIssS) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -264,13 +277,15 @@ __global__ void __launch_bounds__(768, 1)
       for (int i = max(0, kvc - 2); i < kvc; ++i) drain_wait(&b.kv_full[i & 1], (i >> 1) & 1);
       for (int i = max(0, qc - ST); i < qc; ++i) drain_wait(&b.q_full[i % ST], (i / ST) & 1);
     }
-  } else if (warp == C::kSIssuer || warp == C::kGIssuer) {
+  } else if (warp >= C::kIssS && warp <= C::kIssLast) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads share the tensor pipe: one issues S^T / dP^T, the other
-    // the gradient products, so the waits of one stream are covered by the
-    // other's MMAs (a thread that waits issues nothing, and the pipe holds
-    // little more than the MMA it is executing).
+    // Five issuing threads, one per product and accumulator: a single thread
+    // issues at most one tcgen05.mma per ~130 cycles whatever the shape (measured
+    // on GB300), while the pipe itself takes one every ~46-55 cycles at N = 32 /
+    // 64 when several threads feed it.  Each accumulator has one issuer, so every
+    // sum runs in a fixed order and results stay bitwise reproducible.
     if (lane == 0) {
+      const int role = warp - C::kIssS;
       // S^T = K Q^T, dP^T = V dO^T: positions x channels tiles, MN-major, K = channels
       const uint64_t dK0 = desc_mnmajor(tile_view<true, DQK>(sbase + C::OFF_K, C::BK), 0);
       const uint64_t dV0 = desc_mnmajor(tile_view<true, DV>(sbase + C::OFF_V, C::BK), 0);
@@ -283,10 +298,8 @@ __global__ void __launch_bounds__(768, 1)
           desc_kmajor(tile_view<true, DV>(sbase + C::OFF_STAGE + C::Q_BYTES, C::BQ), 0);
       const uint64_t dQb0 = desc_kmajor(tile_view<true, DQK>(sbase + C::OFF_STAGE, C::BQ), 0);
       const uint64_t dKb0 = desc_kmajor(tile_view<true, DQK>(sbase + C::OFF_K, C::BK), 0);
-      // P^T / dS^T halves: 128 key rows x 64 queries, K-major; dS of a 128-query
-      // tile: the MN-major view of its two dS^T halves
-      const uint64_t dPT0 = desc_kmajor(SmemTile{sbase + C::OFF_PT, 128, C::BK}, 0);
-      const uint64_t dDST0 = desc_kmajor(SmemTile{sbase + C::OFF_DST, 128, C::BK}, 0);
+      // dS of a 128-query tile: the MN-major view of its two dS^T halves (128 key
+      // rows x 64 queries each, K-major)
       const uint64_t dDS0 = desc_mnmajor(SmemTile{sbase + C::OFF_DST, 128, C::BK}, 0);
       constexpr uint64_t kStep16Rows = (16 * 128) >> 4;
       const uint32_t idS_full = idesc_bf16_f32(128, C::BQ, true, true);
@@ -294,58 +307,81 @@ __global__ void __launch_bounds__(768, 1)
       const uint32_t idDK = idesc_bf16_f32(128, DQK, false, false);
       const uint32_t idDQ = idesc_bf16_f32(128, DQK, true, false);
 
+      // S^T (role 0) or dP^T (role 1) of step s, as soon as the row threads hold
+      // step s - 1's in registers
       auto issue_sdp = [&](int u, int kt, int j) -> bool {
-        const int kvi = u * nkt + kt, s = kvi * nqs + j, st = s % ST, kb = kvi & 1, bb = s & 1;
+        const int kvi = u * nkt + kt, s = kvi * nqs + j, st = s % ST, kb = kvi & 1;
         if ((j == 0 && !mbar_wait(&b.kv_full[kb], (kvi >> 1) & 1, abort)) ||
             !mbar_wait(&b.q_full[st], (s / ST) & 1, abort) ||
-            (s >= 2 && !mbar_wait(&b.s_free[bb], ((s >> 1) - 1) & 1, abort)))
+            (s >= 1 && !mbar_wait(&b.s_free, (s - 1) & 1, abort)))
           return false;
         tc_fence_after();
-        const uint64_t dK = dK0 + (uint64_t)(kb * C::K_BYTES >> 4);
-        const uint64_t dV = dV0 + (uint64_t)(kb * C::V_BYTES >> 4);
-        const uint64_t dQ = dQ0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
-        const uint64_t dDO = dDO0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
         const int vq = min(C::BQ, N - j * C::BQ);
         const uint32_t id = vq == C::BQ ? idS_full : idesc_bf16_f32(128, (vq + 15) & ~15, true, true);
-        const uint32_t tS = tmem + C::TM_S + 64 * bb, tP = tmem + C::TM_DP + 64 * bb;
+        if (role == 0) {
+          const uint64_t dK = dK0 + (uint64_t)(kb * C::K_BYTES >> 4);
+          const uint64_t dQ = dQ0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk)
-          mma_bf16(tS, dK + kk * kStep16Rows, dQ + kk * kStep16Rows, id, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            mma_bf16(tmem + C::TM_S, dK + kk * kStep16Rows, dQ + kk * kStep16Rows, id, kk > 0 ? 1u : 0u);
+        } else {
+          const uint64_t dV = dV0 + (uint64_t)(kb * C::V_BYTES >> 4);
+          const uint64_t dDO = dDO0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk)
-          mma_bf16(tP, dV + kk * kStep16Rows, dDO + kk * kStep16Rows, id, kk > 0 ? 1u : 0u);
-        mma_commit(&b.s_full[bb]);
+          for (int kk = 0; kk < DV / 16; ++kk)
+            mma_bf16(tmem + C::TM_DP, dV + kk * kStep16Rows, dDO + kk * kStep16Rows, id, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&b.s_full);
+        mma_commit(&b.q_empty[st]);
+        if (j == nqs - 1) mma_commit(&b.kv_empty[kb]);
         return true;
       };
-      auto issue_grad = [&](int u, int kt, int j) -> bool {
-        const int kvi = u * nkt + kt, s = kvi * nqs + j, st = s % ST, kb = kvi & 1, bb = s & 1;
+      // dV += P^T dO (role 2) or dK += dS^T Q (role 3) of step s, A from TMEM
+      auto issue_dvdk = [&](int u, int kt, int j) -> bool {
+        const int kvi = u * nkt + kt, s = kvi * nqs + j, st = s % ST, bb = s & 1;
+        if (!mbar_wait(&b.p_full[bb], (s >> 1) & 1, abort) ||
+            !mbar_wait(&b.q_full[st], (s / ST) & 1, abort) ||
+            (j == 0 && kvi >= 1 && !mbar_wait(&b.acc_free, (kvi - 1) & 1, abort)))
+          return false;
+        tc_fence_after();
+        const int vq = min(C::BQ, N - j * C::BQ);
+        if (role == 2) {
+          const uint64_t dDOb = dDOb0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
+          const uint32_t tPT = tmem + C::TM_PT + 32 * bb;  // 8 columns per 16 queries
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            if (kk * 16 < vq)
+              mma_bf16_ts(tmem + C::TM_DV, tPT + 8 * kk, dDOb + 2 * kk, idDV, (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          const uint64_t dQb = dQb0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
+          const uint32_t tDST = tmem + C::TM_DST + 32 * bb;
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            if (kk * 16 < vq)
+              mma_bf16_ts(tmem + C::TM_DK, tDST + 8 * kk, dQb + 2 * kk, idDK, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&b.q_empty[st]);
+        mma_commit(&b.g_done[bb]);
+        if (j == nqs - 1) mma_commit(&b.acc_full);
+        return true;
+      };
+      // dQ_t += dS K (role 4) once both halves of query tile t (or its only one)
+      // are stored; every step, so that g_done counts this thread's reads of the
+      // dS^T pair buffers
+      auto issue_dq = [&](int u, int kt, int j) -> bool {
+        const int kvi = u * nkt + kt, s = kvi * nqs + j, kb = kvi & 1, bb = s & 1;
         // the first dQ product of a head overwrites the accumulators the epilogue
         // warps read out for the previous head
         const bool dq_step = (j & 1) || j == nqs - 1;
         const bool first_dq = kt == 0 && dq_step && j <= 1;
         if (!mbar_wait(&b.p_full[bb], (s >> 1) & 1, abort) ||
-            (j == 0 && kvi >= 1 && !mbar_wait(&b.acc_free, (kvi - 1) & 1, abort)) ||
+            (j == 0 && !mbar_wait(&b.kv_full[kb], (kvi >> 1) & 1, abort)) ||
             (first_dq && u >= 1 && !mbar_wait(&b.dq_free, (u - 1) & 1, abort)))
           return false;
         tc_fence_after();
-        const int qt = j >> 1, pi = kvi * nqt + qt, pb = pi & 1;
-        const uint64_t dDOb = dDOb0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
-        const uint64_t dQb = dQb0 + (uint64_t)(st * C::STAGE_BYTES >> 4);
-        const uint64_t dPT = dPT0 + (uint64_t)(bb * C::HALF_BYTES >> 4);
-        const uint64_t dDST =
-            dDST0 + (uint64_t)((pb * C::PAIR_BYTES + (j & 1) * C::HALF_BYTES) >> 4);
-        const int vq = min(C::BQ, N - j * C::BQ), vk = min(C::BK, N - kt * C::BK);
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          if (kk * 16 < vq)
-            mma_bf16(tmem + C::TM_DV, dPT + 2 * kk, dDOb + 2 * kk, idDV, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          if (kk * 16 < vq)
-            mma_bf16(tmem + C::TM_DK, dDST + 2 * kk, dQb + 2 * kk, idDK, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&b.q_empty[st]);
-        // dQ of the 128-query tile once both of its halves (or its only one) are stored
         if (dq_step) {
+          const int qt = j >> 1, pb = (kvi * nqt + qt) & 1;
+          const int vk = min(C::BK, N - kt * C::BK);
           const uint64_t dDS = dDS0 + (uint64_t)(pb * C::PAIR_BYTES >> 4);
           const uint64_t dKb = dKb0 + (uint64_t)(kb * C::K_BYTES >> 4);
 #pragma unroll
@@ -358,7 +394,6 @@ __global__ void __launch_bounds__(768, 1)
         mma_commit(&b.g_done[bb]);
         if (j == nqs - 1) {
           mma_commit(&b.kv_empty[kb]);
-          mma_commit(&b.acc_full);
           if (kt == nkt - 1) mma_commit(&b.dq_full);
         }
         return true;
@@ -369,9 +404,9 @@ __global__ void __launch_bounds__(768, 1)
       for (int u = 0; ok && u < nunits; ++u)
         for (int kt = 0; ok && kt < nkt; ++kt)
           for (int j = 0; ok && j < nqs; ++j)
-            ok = warp == C::kSIssuer ? issue_sdp(u, kt, j) : issue_grad(u, kt, j);
-      mma_commit(&b.mma_done[warp - C::kSIssuer]);
-      drain_wait(&b.mma_done[warp - C::kSIssuer], 0);
+            ok = role <= 1 ? issue_sdp(u, kt, j) : role <= 3 ? issue_dvdk(u, kt, j) : issue_dq(u, kt, j);
+      mma_commit(&b.mma_done[role]);
+      drain_wait(&b.mma_done[role], 0);
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue warps
@@ -516,7 +551,7 @@ __global__ void __launch_bounds__(768, 1)
           const int vq = min(C::BQ, N - j * C::BQ);
           const int mine = vq - c0;
           const bool active = krows && mine > 0;
-          if (!mbar_wait(&b.s_full[bb], (s >> 1) & 1, abort)) {
+          if (!mbar_wait(&b.s_full, s & 1, abort)) {
             ok = false;
             break;
           }
@@ -524,33 +559,30 @@ __global__ void __launch_bounds__(768, 1)
           uint32_t pw[8], dw[8];  // packed P^T and dS^T of this thread's 16 queries
           if (active) {
             uint32_t sv[16], pv[16];
-            tmem_load16_async(tmem + lane_base + C::TM_S + 64 * bb + c0, sv);
-            tmem_load16_async(tmem + lane_base + C::TM_DP + 64 * bb + c0, pv);
+            tmem_load16_async(tmem + lane_base + C::TM_S + c0, sv);
+            tmem_load16_async(tmem + lane_base + C::TM_DP + c0, pv);
             tmem_wait_ld();
             tmem_pin(sv);
             tmem_pin(pv);
             tc_fence_before();
-            mbar_arrive(&b.s_free[bb]);
+            mbar_arrive(&b.s_free);
             const float* lrow = hst + j * C::BQ + c0;
             p_ds_chunk<16>(sv, pv, lrow, lrow + C::MAXN, sl2, pw, dw);
           } else {
             tc_fence_before();
-            mbar_arrive(&b.s_free[bb]);
+            mbar_arrive(&b.s_free);
           }
-          // P^T buffer s & 1 was last read by the products of step s - 2, and the
-          // dS^T pair buffer by those of step s - 3 or s - 4: all done once the
-          // products of step s - 2 are (one issuing thread, commits cover all
-          // earlier MMAs)
+          // the P^T / dS^T TMEM buffers s & 1 were last read by the products of
+          // step s - 2, and the dS^T pair buffer by those of step s - 3 or s - 4:
+          // all done once the products of step s - 2 are (one issuing thread,
+          // commits cover all earlier MMAs)
           if (s >= 2 && !mbar_wait(&b.g_done[bb], ((s >> 1) - 1) & 1, abort)) {
             ok = false;
             break;
           }
           if (active) {
-            const uint32_t pt = sbase + C::OFF_PT + bb * C::HALF_BYTES;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-              st_shared_v4(pt + swizzled_offset(r, c0 / 8 + i, 128), pw[4 * i], pw[4 * i + 1],
-                           pw[4 * i + 2], pw[4 * i + 3]);
+            tmem_store8_async(tmem + lane_base + C::TM_PT + 32 * bb + c0 / 2, pw);
+            tmem_store8_async(tmem + lane_base + C::TM_DST + 32 * bb + c0 / 2, dw);
           }
           if (active) {
             const uint32_t half = sbase + C::OFF_DST + pb * C::PAIR_BYTES + (j & 1) * C::HALF_BYTES;
@@ -559,6 +591,7 @@ __global__ void __launch_bounds__(768, 1)
               st_shared_v4(half + swizzled_offset(r, c0 / 8 + i, 128), dw[4 * i], dw[4 * i + 1],
                            dw[4 * i + 2], dw[4 * i + 3]);
           }
+          if (active) tmem_wait_st();
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&b.p_full[bb]);
@@ -571,7 +604,7 @@ __global__ void __launch_bounds__(768, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == C::kSIssuer) {
+  if (warp == C::kIssS) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
