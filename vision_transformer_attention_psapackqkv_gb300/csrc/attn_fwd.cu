@@ -13,12 +13,13 @@
 //                      (split rows: warps 0-7 of the single slot, see below)
 //   next warp (P)      TMA producer: per slot, Q (double- or single-buffered)
 //                      and a 2- to 4-stage ring of 64-key K/V tiles
-//   warp P + 1         MMA issuer (one thread) and TMEM owner; per slot
-//                        S_k = Q K_k^T -> TMEM (64 columns)
-//                        O  += P_k V_k -> TMEM (DV columns), P_k read from
-//                        tensor memory (A operand; double-buffered)
-//                      S_{k+1} is issued as soon as the softmax holds S_k in
-//                      registers, so it overlaps the exponentials of tile k.
+//   warp P + 1         S issuer (one thread) and TMEM owner; per slot
+//                        S_k = Q K_k^T -> TMEM (64 columns), issued as soon as
+//                        the softmax holds S_{k-1} in registers, so it overlaps
+//                        the exponentials of tile k-1
+//   warp P + 2         P.V issuer (one thread): O += P_k V_k -> TMEM (DV
+//                      columns), P_k read from tensor memory (A operand;
+//                      double-buffered)
 // The bf16 kernels run persistent grids; with one slot per CTA two CTAs share
 // an SM (and its tensor core), which interleaves their softmax and MMA phases.
 // Split rows (kSplit, short sequences): warps 0-3 and 4-7 both cover the 128 rows,
@@ -68,9 +69,10 @@ struct FwdCfg {
   static constexpr int HC = BN / H;         // S columns per softmax thread
   static constexpr int kRowThreads = 128 * H;  // softmax threads of a slot
   static constexpr int kSoftmaxWarps = 4 * NWG * H;
-  // control warps: TMA producer, MMA issuer (TMEM owner)
+  // control warps: TMA producer, S issuer (TMEM owner), P.V issuer
   static constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
-  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;
+  static constexpr int kPvWarp = kSoftmaxWarps + 2;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 96;
   static constexpr uint32_t Q_BYTES = BM * DQK * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2;
   static constexpr uint32_t V_BYTES = BN * DV * 2;
@@ -186,7 +188,7 @@ __device__ __forceinline__ int slot_tiles(int slot, int nslots, int T) {
 }
 
 template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
-__global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 2 : 1)
+__global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 2 : 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQK,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -195,8 +197,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
   unsigned char* smem = align1024(smem_raw);
   const uint32_t sbase = smem_addr(smem);
   SlotBars* bars = reinterpret_cast<SlotBars*>(smem + C::OFF_BAR);
-  uint64_t* mma_done = reinterpret_cast<uint64_t*>(bars + NWG);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* mma_done = reinterpret_cast<uint64_t*>(bars + NWG);  // one per issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
       }
       for (int i = 0; i < C::STAGES; ++i) {
         mbar_init(&b.kv_full[i], 1);
-        mbar_init(&b.kv_empty[i], 1);
+        mbar_init(&b.kv_empty[i], 2);  // K read by S, V by P.V: one commit each
       }
       mbar_init(&b.s_full, 1);
       mbar_init(&b.s_free, C::kRowThreads);
@@ -227,7 +229,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
       mbar_init(&b.o_free, C::kRowThreads);
       mbar_init(&b.ml_ready, C::kRowThreads);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -332,9 +335,13 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
         }
       }
     }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == C::kMmaWarp || warp == C::kPvWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // S and P.V are issued by two threads: one thread issues at most one
+    // tcgen05.mma per ~130 cycles whatever its shape (measured), so S of the next
+    // tile does not queue behind the four P.V products of this one.
     if (lane == 0) {
+      const bool s_role = warp == C::kMmaWarp;
       // descriptors of buffer 0 / stage 0 of slot 0; the others are fixed offsets
       const uint64_t dQ0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_Q, C::BM), 0);
       const uint64_t dK0 = desc_pos_by_ch<kNCHW>(tile_view<kNCHW, DQK>(sbase + C::SL_K, C::BN), 0);
@@ -362,6 +369,7 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
           mma_bf16(tmem + w * C::TM_SLOT, dQ + kk * kStepQK, dK + kk * kStepQK, idS,
                    kk > 0 ? 1u : 0u);
         mma_commit(&b.s_full);
+        mma_commit(&b.kv_empty[k % C::STAGES]);
         if (j == nkv - 1) mma_commit(&b.q_empty[i % QBUF]);
         return true;
       };
@@ -395,19 +403,13 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 64, NWG == 1 ? 
         return true;
       };
       bool ok = true;
-      for (int i = 0; ok && i < max_tiles; ++i) {
-        for (int w = 0; ok && w < NWG; ++w)
-          if (i < ntiles[w]) ok = issue_s(w, i, 0);
-        for (int j = 0; ok && j < nkv; ++j) {
-          if (j + 1 < nkv)
-            for (int w = 0; ok && w < NWG; ++w)
-              if (i < ntiles[w]) ok = issue_s(w, i, j + 1);
+      for (int i = 0; ok && i < max_tiles; ++i)
+        for (int j = 0; ok && j < nkv; ++j)
           for (int w = 0; ok && w < NWG; ++w)
-            if (i < ntiles[w]) ok = issue_pv(w, i, j);
-        }
-      }
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);  // every MMA retired before TMEM is released
+            if (i < ntiles[w]) ok = s_role ? issue_s(w, i, j) : issue_pv(w, i, j);
+      uint64_t* done = &mma_done[s_role ? 0 : 1];
+      mma_commit(done);
+      drain_wait(done, 0);  // every MMA retired before TMEM is released
     }
   }
   } else {
