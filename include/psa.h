@@ -160,10 +160,17 @@ psa_status_t psa_attention_fwd_residual(const void *qkv_nchw, void *out_res_nchw
 /* Backward of psa_attention_fwd: given qkv, the forward's out and lse, the
  * upstream gradient dout [B, c, H, W] and optionally the gradient dvres of the
  * extracted V (nullable), writes dqkv_nchw [B, qkv_h, H, W] (overwritten, V
- * channels include dvres).  workspace must hold
- * psa_attention_bwd_workspace_size(shape) bytes (device, 16-byte aligned); for
- * key_dim 32 and N <= 512 one kernel computes delta on chip and leaves the
- * workspace untouched.  bf16 only; key_dim 32 or 64. */
+ * channels include dvres).  workspace is device memory, 16-byte aligned, of
+ * ws_bytes >= psa_attention_bwd_workspace_size(shape) bytes.  Which kernels run:
+ *   - key_dim 32, bf16, N <= 512: one kernel per head computes delta on chip and
+ *     forms every P and dS once; the workspace is not touched;
+ *   - key_dim 32, bf16, 512 < N <= 2048, with the full workspace: the same kernel,
+ *     with the dQ accumulator in the workspace;
+ *   - otherwise (key_dim 64, longer N, or a workspace of only B*num_heads*N*4
+ *     bytes rounded up to 256, the least accepted): the dQ and dK/dV kernels of
+ *     the two-kernel form, with delta in the workspace;
+ *   - fp32, or rows that are not 16-byte multiples: CUDA-core dQ and dK/dV.
+ * key_dim 32 or 64; bf16 or fp32. */
 psa_status_t psa_attention_bwd(const void *qkv_nchw, const void *out_nchw, const void *dout_nchw,
                                const float *lse, const void *dvres_nchw, void *dqkv_nchw,
                                void *workspace, size_t ws_bytes, psa_shape_t shape, float scale,
@@ -198,19 +205,24 @@ psa_status_t psa_attention_bwd_dkdv(const void *qkv_nchw, const void *dout_nchw,
  * invalid shape (PSA_ERR_INVALID_ARG), then that limit (PSA_ERR_UNSUPPORTED),
  * then every other check of psa_attention_bwd.  The first call on each device,
  * made with that device current, looks up the array's address; make that first
- * call before any stream capture.  Only the two-kernel form of the backward
- * (key_dim 64, or N > 512) uses the array; the one-kernel form (key_dim 32,
- * N <= 512) keeps delta on chip.  All calls of the two-kernel form share the one
- * array: such calls whose kernels overlap on the GPU (other streams, other
- * threads) race on it, so serialise them.  Nothing in the array needs clearing
- * between calls (each call writes every value it reads).  No allocation of any
- * kind is made. */
+ * call before any stream capture.  The array serves as the workspace of
+ * psa_attention_bwd: it holds delta for the two-kernel form (key_dim 64, fp32,
+ * rows that are not 16-byte multiples, or N > 2048), or the dQ accumulator of the
+ * one-kernel form for key_dim 32 and 512 < N <= 2048 when B * num_heads * N * 32
+ * floats fit in it (the two-kernel form otherwise); the one-kernel form for
+ * N <= 512 keeps everything on chip and leaves it untouched.  All calls that use
+ * the array share it: such calls whose kernels overlap on the GPU (other
+ * streams, other threads) race on it, so serialise them.  Nothing in the array
+ * needs clearing between calls (each call writes every value it reads before it
+ * reads it).  No allocation of any kind is made. */
 psa_status_t psa_attention_bwd_noalloc(const void *qkv_nchw, const void *out_nchw,
                                        const void *dout_nchw, const float *lse,
                                        const void *dvres_nchw, void *dqkv_nchw, psa_shape_t shape,
                                        float scale, cudaStream_t stream);
 
-/* Bytes of device workspace psa_attention_bwd needs (0 for an invalid shape). */
+/* Bytes of device workspace for psa_attention_bwd to take its fastest form (0 for
+ * an invalid shape): B*num_heads*N*4 rounded up to 256 (delta), or, for key_dim 32
+ * and 512 < N <= 2048, B*num_heads*N*32*4 rounded up to 256 (a dQ accumulator). */
 size_t psa_attention_bwd_workspace_size(psa_shape_t shape);
 
 /* ---- status ------------------------------------------------------------------- */

@@ -101,6 +101,9 @@ RAGGED = [
     # KD = 32 around the one-kernel backward's tiles and its limit: N = 128, 512, 520;
     # around the single-pass forward's limit: N = 448, 456
     (2, 1, 32, 8, 16), (1, 2, 32, 16, 32), (1, 1, 32, 4, 130), (1, 2, 32, 16, 28), (1, 1, 32, 8, 57),
+    # the one-kernel backward beyond 512 positions (dQ accumulated in the workspace):
+    # N = 1032 (a 16-position last query step), 2048 (its limit); N = 2056 is past it
+    (1, 1, 32, 8, 129), (1, 2, 32, 32, 64), (1, 1, 32, 8, 257),
 ]
 
 

@@ -4,9 +4,11 @@ device allocation, or a latency-critical loop where cudaMalloc / cudaFree would
 synchronise the device).  Its delta scratch is a fixed array inside the library,
 so the caller passes only inputs and outputs.
 
-The backward keeps delta in that array only in its two-kernel form (key_dim 64, or
-more than 512 positions), so the cases below use that form, on two different
-shapes called one after the other, plus one one-kernel case.  Each call is made
+The backward uses that array as its workspace: for delta in its two-kernel form
+(key_dim 64 below), and as the dQ accumulator of its one-kernel form between 512
+and 2048 positions (N = 1600 below); up to 512 positions it leaves the array
+alone.  The cases run those forms on different shapes one after the other, plus
+one short case.  Each call is made
 twice in a row through the C ABI, and each result is compared with the fp64
 oracle at the bf16 bars the other tests use, and bit for bit with
 psa_attention_bwd given a workspace of its own.  This file is collected last on
@@ -25,7 +27,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # (B, nh, KD, H, W, seed)
     (2, 2, 64, 20, 20, 77),   # key_dim 64: dQ kernel writes delta, dK/dV kernel reads it
-    (1, 2, 32, 40, 40, 78),   # N = 1600 > 512: the same two kernels
+    (1, 2, 32, 40, 40, 78),   # N = 1600: one kernel, dQ accumulated in the array
     (2, 2, 64, 8, 12, 79),    # a smaller two-kernel case right after a larger one
     (2, 4, 32, 20, 20, 80),   # key_dim 32, N = 400: one kernel, delta on chip
 ]

@@ -455,10 +455,29 @@ psa_status_t psa_attention_fwd_residual(const void* qkv, void* out_res, void* ou
   return fused_fwd(qkv, out, lse, nullptr, out_res, s, scale, st);
 }
 
+namespace {
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// delta [BH, N] fp32: what the two-kernel backward needs
+size_t delta_ws_bytes(const psa_shape_t& s) {
+  return round256((size_t)s.B * s.num_heads * s.H * s.W * sizeof(float));
+}
+
+// the dQ accumulator [BH, N, 32] fp32 of the one-kernel backward beyond
+// kFusedBwdMaxN positions (0 where that form does not apply)
+size_t long_fused_ws_bytes(const psa_shape_t& s) {
+  const long long N = (long long)s.H * s.W;
+  if (s.key_dim != 32 || s.dtype != PSA_DTYPE_BF16 || (N * 2) % 16 != 0 ||
+      N <= psa::kFusedBwdMaxN || N > psa::kFusedBwdMaxNLong)
+    return 0;
+  return round256((size_t)s.B * s.num_heads * N * 32 * sizeof(float));
+}
+}  // namespace
+
 size_t psa_attention_bwd_workspace_size(psa_shape_t s) {
   if (check_shape(s) != PSA_OK) return 0;
-  // delta [BH, N] fp32
-  return ((size_t)s.B * s.num_heads * s.H * s.W * sizeof(float) + 255) & ~(size_t)255;
+  const size_t a = delta_ws_bytes(s), b = long_fused_ws_bytes(s);
+  return a > b ? a : b;
 }
 
 namespace {
@@ -563,7 +582,7 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
   if (!ws) return PSA_ERR_INVALID_ARG;
   psa_status_t e = check_shape(s);
   if (e != PSA_OK) return e;
-  if (ws_bytes < psa_attention_bwd_workspace_size(s)) return PSA_ERR_INVALID_ARG;
+  if (ws_bytes < delta_ws_bytes(s)) return PSA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
   // validate both launches completely before issuing either
   CUtensorMap mqk, mv, mdo, mo, mqk2, mv2, mdo2;
@@ -586,9 +605,12 @@ psa_status_t psa_attention_bwd(const void* qkv, const void* out, const void* dou
                  &a_kv);
   if (e != PSA_OK) return e;
   const int BH = s.B * s.num_heads;
-  if (s.key_dim == 32 && s.H * s.W <= psa::kFusedBwdMaxN) {
-    // short sequences: one kernel per head produces delta, dQ, dK and dV from a
-    // single walk over its tiles (the workspace is not used)
+  const size_t long_ws = long_fused_ws_bytes(s);
+  if (s.key_dim == 32 &&
+      (s.H * s.W <= psa::kFusedBwdMaxN || (long_ws > 0 && ws_bytes >= long_ws))) {
+    // one kernel per head produces delta, dQ, dK and dV from a single walk over
+    // its tiles (the workspace holds the dQ accumulator beyond kFusedBwdMaxN
+    // positions and is not used below)
     a_dq.dvres = static_cast<const __nv_bfloat16*>(dvres);
     return from_cuda(psa::launch_psa_bwd_fused(mqk, mv, mdo, a_dq, s.key_dim, st));
   }

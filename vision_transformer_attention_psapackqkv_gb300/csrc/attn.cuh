@@ -110,10 +110,13 @@ cudaError_t launch_psa_bwd_dkdv(const CUtensorMap& mQK, const CUtensorMap& mV,
                                 const CUtensorMap& mDO, const BwdArgs& a, int BH, int KD,
                                 cudaStream_t st);
 
-// Backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxN, N % 8 == 0):
-// one kernel computes delta (from a.o and a.dO, on chip; a.delta is not used), dQ,
-// dK and dV.  Same maps as launch_psa_bwd_dkdv.
+// Backward of a whole head per CTA (NCHW, KD = 32, N <= kFusedBwdMaxNLong,
+// N % 8 == 0): one kernel computes delta (from a.o and a.dO, on chip), dQ, dK and
+// dV.  Up to kFusedBwdMaxN positions a.delta is not used; beyond, a.delta points
+// at an fp32 workspace of BH * N * 32 floats that accumulates dQ.  Same maps as
+// launch_psa_bwd_dkdv.
 constexpr int kFusedBwdMaxN = 512;
+constexpr int kFusedBwdMaxNLong = 2048;
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
                                  const CUtensorMap& mDO, const BwdArgs& a, int KD,
                                  cudaStream_t st);

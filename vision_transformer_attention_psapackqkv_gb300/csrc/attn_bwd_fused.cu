@@ -95,9 +95,15 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[NC], const uint3
   }
 }
 
-template <int DQK, int DV, int ST>
+// kLong: up to kFusedBwdMaxNLong positions; dQ of each 128-query tile and key
+// tile is a partial sum that the epilogue warps add into an fp32 accumulator in
+// the workspace, in key-tile order.  Otherwise (up to kFusedBwdMaxN positions)
+// dQ of every query tile stays in tensor memory for the whole head.
+template <int DQK, int DV, int ST, bool kLong>
 struct FusedCfg {
-  static constexpr int BK = 128, BQ = 64, QT = 128, MAXN = kFusedBwdMaxN, MAXQT = MAXN / QT;
+  static constexpr int BK = 128, BQ = 64, QT = 128;
+  static constexpr int MAXN = kLong ? kFusedBwdMaxNLong : kFusedBwdMaxN, MAXQT = MAXN / QT;
+  static constexpr int CHUNK = 512;  // positions per pass of the delta computation
   static constexpr int kRowWarps = 16, kThreads = 32 * kRowWarps + 384;
   // producer, then the issuers of S^T (TMEM owner), dP^T, dV, dK and dQ, two idle
   // warps, then four epilogue warps (warp % 4 = TMEM lane quadrant)
@@ -114,14 +120,16 @@ struct FusedCfg {
   static constexpr uint32_t OFF_DST = OFF_STAGE + ST * STAGE_BYTES;  // dS^T: two pair buffers
   static constexpr uint32_t OFF_HSTAT = OFF_DST + 2 * PAIR_BYTES;  // two heads
   static constexpr uint32_t OFF_DSCR = OFF_HSTAT + 2 * HSTAT_BYTES;  // delta partial sums
-  static constexpr uint32_t OFF_BAR = OFF_DSCR + 8 * MAXN * 4;
+  static constexpr uint32_t OFF_BAR = OFF_DSCR + 8 * CHUNK * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
   // TMEM columns: S^T, dP^T (fp32), then P^T_b and dS^T_b (bf16 pairs, 32 columns
-  // per 64 queries, b = step parity), dV, dK, dQ of up to 4 query tiles
+  // per 64 queries, b = step parity), dV, dK, then dQ: of up to 4 query tiles, or
+  // (kLong) two buffers of one query tile's partial sum
   static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_PT = 128, TM_DST = 192;
   static constexpr uint32_t TM_DV = 256, TM_DK = TM_DV + DV;
   static constexpr uint32_t TM_DQ = TM_DK + DQK;
-  static_assert(TM_DQ + MAXQT * DQK <= 512, "tensor memory");
+  static_assert(TM_DQ + (kLong ? 2 : MAXQT) * DQK <= 512, "tensor memory");
+  static_assert(MAXN % CHUNK == 0 && 8 * 64 == CHUNK, "delta passes of 512 positions");
   static_assert(SMEM_BYTES <= 227 * 1024 && SMEM_BYTES > 114 * 1024, "one CTA per SM");
   static_assert(kEpiWarp0 % 4 == 0, "epilogue warps cover the four lane quadrants in order");
   static_assert(ST >= 2 && ST <= 8, "stages");
@@ -130,7 +138,7 @@ struct FusedCfg {
 struct FusedBars {
   uint64_t kv_full[2], kv_empty[2], q_full[8], q_empty[8];
   uint64_t s_full, s_free, p_full[2], g_done[2], hs_full[2], hs_free[2];
-  uint64_t acc_full, acc_free, dq_full, dq_free, mma_done[5];
+  uint64_t acc_full, acc_free, dq_full[2], dq_free[2], mma_done[5];
   uint64_t dl_part, dl_full;  // a head's delta: partial sums written, delta written
 };
 static_assert(sizeof(FusedBars) + 8 <= 512, "barrier area");
@@ -142,13 +150,13 @@ __device__ __forceinline__ uint64_t off_ch_by_pos(int kk) {
   return (uint64_t)((kk >> 2) * ((D * 128) >> 4) + (kk & 3) * (32 >> 4));
 }
 
-template <int DQK, int DV, int ST>
+template <int DQK, int DV, int ST, bool kLong>
 __global__ void __launch_bounds__(896, 1)
     attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ CUtensorMap tmDO, const BwdArgs args) {
-  using C = FusedCfg<DQK, DV, ST>;
+  using C = FusedCfg<DQK, DV, ST, kLong>;
   static_assert(DQK == 32 && DV == 64, "tile split of the epilogue");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -191,8 +199,10 @@ __global__ void __launch_bounds__(896, 1)
     }
     mbar_init(&b.acc_full, 2);
     mbar_init(&b.acc_free, C::kEpiThreads);
-    mbar_init(&b.dq_full, 1);
-    mbar_init(&b.dq_free, C::kEpiThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.dq_full[i], 1);
+      mbar_init(&b.dq_free[i], C::kEpiThreads);
+    }
     mbar_init(&b.dl_part, 32 * C::kRowWarps);
     mbar_init(&b.dl_full, 32 * C::kRowWarps);
     *abort = 0;
@@ -214,23 +224,22 @@ __global__ void __launch_bounds__(896, 1)
   if (warp == C::kProducer) {
     // ------------------------------------------------------------ TMA producer
     // K / V and Q / dO by lane 0.  The negated lse2 of a whole head is written to
-    // shared memory by all lanes (double-buffered by head parity) from their
-    // registers (query lane + 32 i), which are loaded one head ahead, so no
-    // global-memory latency lands between two stages.  (The row threads add the
-    // head's delta.)
+    // shared memory by all lanes (double-buffered by head parity); its first 512
+    // positions come from registers (query lane + 32 i) loaded one head ahead, so
+    // no global-memory latency lands between two stages.  (The row threads add
+    // the head's delta.)
     bool ok = true;
     int kvc = 0, qc = 0;
-    constexpr int kPer = C::MAXN / 32;
+    constexpr int kPer = C::CHUNK / 32;
     float nl[kPer];
-    auto load_head = [&](int u) {
-      const int bh = head_of(u);
+    auto load_chunk = [&](int bh, int c0) {
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const int q = lane + 32 * i;
+        const int q = c0 + lane + 32 * i;
         nl[i] = q < N ? -args.lse[(long long)bh * N + q] * kLog2e : -INFINITY;
       }
     };
-    if (nunits > 0) load_head(0);
+    if (nunits > 0) load_chunk(head_of(0), 0);
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
       if (u >= 2 && !mbar_wait(&b.hs_free[u & 1], ((u >> 1) - 1) & 1, abort)) {
@@ -238,10 +247,13 @@ __global__ void __launch_bounds__(896, 1)
         break;
       }
       float* hst = reinterpret_cast<float*>(smem + C::OFF_HSTAT + (u & 1) * C::HSTAT_BYTES);
+      for (int c0 = 0; c0 < C::MAXN; c0 += C::CHUNK) {
+        if (c0 > 0) load_chunk(bh, c0);
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) hst[lane + 32 * i] = nl[i];
+        for (int i = 0; i < kPer; ++i) hst[c0 + lane + 32 * i] = nl[i];
+      }
       mbar_arrive(&b.hs_full[u & 1]);
-      if (u + 1 < nunits) load_head(u + 1);
+      if (u + 1 < nunits) load_chunk(head_of(u + 1), 0);
       for (int kt = 0; ok && kt < nkt; ++kt) {
         const int kb = kvc & 1;
         if (kvc >= 2 && !mbar_wait(&b.kv_empty[kb], ((kvc >> 1) - 1) & 1, abort)) {
@@ -367,34 +379,40 @@ __global__ void __launch_bounds__(896, 1)
       };
       // dQ_t += dS K (role 4) once both halves of query tile t (or its only one)
       // are stored; every step, so that g_done counts this thread's reads of the
-      // dS^T pair buffers
+      // dS^T pair buffers.  kLong: the product of this key tile alone, into one of
+      // two TMEM buffers the epilogue warps add into the workspace
       auto issue_dq = [&](int u, int kt, int j) -> bool {
         const int kvi = u * nkt + kt, s = kvi * nqs + j, kb = kvi & 1, bb = s & 1;
-        // the first dQ product of a head overwrites the accumulators the epilogue
-        // warps read out for the previous head
         const bool dq_step = (j & 1) || j == nqs - 1;
+        const int qt = j >> 1, pi = kvi * nqt + qt, pb = pi & 1;
+        // the first dQ product of a head (or, kLong, of a buffer) overwrites the
+        // accumulators the epilogue warps read out before
         const bool first_dq = kt == 0 && dq_step && j <= 1;
+        const bool wait_free = kLong ? (dq_step && pi >= 2) : (first_dq && u >= 1);
+        const int free_bar = kLong ? pb : 0;
+        const uint32_t free_parity = kLong ? (((pi >> 1) - 1) & 1) : ((u - 1) & 1);
         if (!mbar_wait(&b.p_full[bb], (s >> 1) & 1, abort) ||
             (j == 0 && !mbar_wait(&b.kv_full[kb], (kvi >> 1) & 1, abort)) ||
-            (first_dq && u >= 1 && !mbar_wait(&b.dq_free, (u - 1) & 1, abort)))
+            (wait_free && !mbar_wait(&b.dq_free[free_bar], free_parity, abort)))
           return false;
         tc_fence_after();
         if (dq_step) {
-          const int qt = j >> 1, pb = (kvi * nqt + qt) & 1;
           const int vk = min(C::BK, N - kt * C::BK);
           const uint64_t dDS = dDS0 + (uint64_t)(pb * C::PAIR_BYTES >> 4);
           const uint64_t dKb = dKb0 + (uint64_t)(kb * C::K_BYTES >> 4);
+          const uint32_t dst = tmem + C::TM_DQ + (kLong ? pb : qt) * DQK;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             if (kk * 16 < vk)
-              mma_bf16(tmem + C::TM_DQ + qt * DQK, dDS + kk * kStep16Rows,
-                       dKb + off_ch_by_pos<DQK>(kk), idDQ, (kt > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(dst, dDS + kk * kStep16Rows, dKb + off_ch_by_pos<DQK>(kk), idDQ,
+                       ((!kLong && kt > 0) || kk > 0) ? 1u : 0u);
           }
+          if (kLong) mma_commit(&b.dq_full[pb]);
         }
         mma_commit(&b.g_done[bb]);
         if (j == nqs - 1) {
           mma_commit(&b.kv_empty[kb]);
-          if (kt == nkt - 1) mma_commit(&b.dq_full);
+          if (!kLong && kt == nkt - 1) mma_commit(&b.dq_full[0]);
         }
         return true;
       };
@@ -416,10 +434,56 @@ __global__ void __launch_bounds__(896, 1)
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
     const float sc = args.scale;
     bool ok = true;
+    // dQ rows of query tile qt: the 32 values of this lane, scaled and rounded
+    auto store_dq = [&](int bh, int qt, const float (&acc)[32]) {
+      const int q = qt * C::QT + r;
+      if (q >= N) return;
+      __nv_bfloat16* dst = args.dq + (long long)qkv_row(bh) * N + q;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
+    };
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
       for (int kt = 0; kt < nkt; ++kt) {
         const int kvi = u * nkt + kt;
+        if (kLong) {
+          // this key tile's dQ of every query tile, added in key-tile order into the
+          // fp32 accumulator of the head in the workspace ([BH, N, 32]); the last
+          // key tile writes the result
+          for (int qt = 0; ok && qt < nqt; ++qt) {
+            const int pi = kvi * nqt + qt, pb = pi & 1;
+            if (!mbar_wait(&b.dq_full[pb], (pi >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            float acc[32];
+            tmem_load32(tmem + lane_base + C::TM_DQ + pb * DQK, acc);
+            tc_fence_before();
+            mbar_arrive(&b.dq_free[pb]);
+            const int q = qt * C::QT + r;
+            if (q >= N) continue;
+            float4* part = reinterpret_cast<float4*>(args.delta + ((long long)bh * N + q) * DQK);
+            if (kt > 0) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float4 p4 = part[e];
+                acc[4 * e] += p4.x;
+                acc[4 * e + 1] += p4.y;
+                acc[4 * e + 2] += p4.z;
+                acc[4 * e + 3] += p4.w;
+              }
+            }
+            if (kt < nkt - 1) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                part[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            } else {
+              store_dq(bh, qt, acc);
+            }
+          }
+          if (!ok) break;
+        }
         if (!mbar_wait(&b.acc_full, kvi & 1, abort)) {
           ok = false;
           break;
@@ -427,7 +491,7 @@ __global__ void __launch_bounds__(896, 1)
         tc_fence_after();
         // dV (column groups 0, 1: 32 channels each) and dK (group 2) of this key
         // tile's rows, one group at a time; the accumulators go back to the
-        // gradient issuer as soon as the last group is in registers
+        // gradient issuers as soon as the last group is in registers
         const int key = kt * C::BK + r;
         const bool live = key < N;
 #pragma unroll 1
@@ -456,25 +520,20 @@ __global__ void __launch_bounds__(896, 1)
           }
         }
       }
-      if (!ok) break;
+      if (!ok || kLong) continue;
       // the head's last products are done: dQ of every 128-query tile
-      if (!mbar_wait(&b.dq_full, u & 1, abort)) {
+      if (!mbar_wait(&b.dq_full[0], u & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int qt = 0; qt < nqt; ++qt) {
-        const int q = qt * C::QT + r;
         float acc[32];
         tmem_load32(tmem + lane_base + C::TM_DQ + qt * DQK, acc);
-        if (q < N) {
-          __nv_bfloat16* dst = args.dq + (long long)qkv_row(bh) * N + q;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dst[(long long)e * N] = __float2bfloat16_rn(acc[e] * sc);
-        }
+        store_dq(bh, qt, acc);
       }
       tc_fence_before();
-      mbar_arrive(&b.dq_free);
+      mbar_arrive(&b.dq_free[0]);
     }
   } else if (warp < C::kRowWarps) {
     // ------------------------------------------------------------ row threads
@@ -484,21 +543,22 @@ __global__ void __launch_bounds__(896, 1)
     const int c0 = cq * 16;        // first query column of this thread in a step
     const float sl2 = args.scale_log2;
     bool ok = true;
+    int dlc = 0;  // delta passes done (phase of dl_part / dl_full)
     for (int u = 0; ok && u < nunits; ++u) {
       const int bh = head_of(u);
       float* hst = reinterpret_cast<float*>(smem + C::OFF_HSTAT + (u & 1) * C::HSTAT_BYTES);
-      {
-        // delta[q] = sum_c Out[c, q] dOut[c, q] over the head's DV channels, while
-        // its first tiles load.  Thread t = 64 s + g sums channels 8s .. 8s+7 at
-        // positions 8g .. 8g+7; the eight channel slices meet in a scratch area
-        // of shared memory.
-        static_assert(C::kRowWarps * 32 == C::MAXN && DV == 64, "one thread per 8 x 8 block");
+      // delta[q] = sum_c Out[c, q] dOut[c, q] over the head's DV channels, while
+      // its first tiles load, 512 positions per pass.  Thread t = 64 s + g sums
+      // channels 8s .. 8s+7 at positions 8g .. 8g+7 of the pass; the eight channel
+      // slices meet in a scratch area of shared memory.
+      static_assert(C::kRowWarps * 32 == C::CHUNK && DV == 64, "one thread per 8 x 8 block");
+      for (int c0 = 0; ok && c0 < N; c0 += C::CHUNK) {
         const int t = threadIdx.x, g = t & 63, sl8 = t >> 6;
         float part[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) part[e] = 0.f;
-        if (8 * g < N) {
-          const long long base = ((long long)out_row(bh) + 8 * sl8) * N + 8 * g;
+        if (c0 + 8 * g < N) {
+          const long long base = ((long long)out_row(bh) + 8 * sl8) * N + c0 + 8 * g;
           uint4 ov[8], dv[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -519,24 +579,26 @@ __global__ void __launch_bounds__(896, 1)
           }
         }
         float* scratch = reinterpret_cast<float*>(smem + C::OFF_DSCR);
-        float4* sp = reinterpret_cast<float4*>(scratch + sl8 * C::MAXN + 8 * g);
+        float4* sp = reinterpret_cast<float4*>(scratch + sl8 * C::CHUNK + 8 * g);
         sp[0] = make_float4(part[0], part[1], part[2], part[3]);
         sp[1] = make_float4(part[4], part[5], part[6], part[7]);
         mbar_arrive(&b.dl_part);
-        if (!mbar_wait(&b.dl_part, u & 1, abort)) {
+        if (!mbar_wait(&b.dl_part, dlc & 1, abort)) {
           ok = false;
           break;
         }
         float dsum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) dsum += scratch[k * C::MAXN + t];
-        hst[C::MAXN + t] = t < N ? -dsum : 0.f;
+        for (int k = 0; k < 8; ++k) dsum += scratch[k * C::CHUNK + t];
+        hst[C::MAXN + c0 + t] = c0 + t < N ? -dsum : 0.f;
         mbar_arrive(&b.dl_full);
-        if (!mbar_wait(&b.dl_full, u & 1, abort)) {
+        if (!mbar_wait(&b.dl_full, dlc & 1, abort)) {
           ok = false;
           break;
         }
+        ++dlc;
       }
+      if (!ok) break;
       if (!mbar_wait(&b.hs_full[u & 1], (u >> 1) & 1, abort)) {
         ok = false;
         break;
@@ -615,15 +677,24 @@ __global__ void __launch_bounds__(896, 1)
 cudaError_t launch_psa_bwd_fused(const CUtensorMap& mQK, const CUtensorMap& mV,
                                  const CUtensorMap& mDO, const BwdArgs& a, int KD,
                                  cudaStream_t st) {
-  if (KD != 32 || a.N > kFusedBwdMaxN || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.o || !a.dO)
+  if (KD != 32 || a.N > kFusedBwdMaxNLong || a.N <= 0 || a.N % 8 != 0 || a.BH <= 0 || !a.o ||
+      !a.dO || (a.N > kFusedBwdMaxN && !a.delta))
     return cudaErrorInvalidValue;
-  using Cfg = FusedCfg<32, 64, 4>;
-  auto kern = attn_bwd_fused_kernel<32, 64, 4>;
+  const int ctas = std::min(device_sm_count(), a.BH);
+  if (a.N <= kFusedBwdMaxN) {
+    using Cfg = FusedCfg<32, 64, 4, false>;
+    auto kern = attn_bwd_fused_kernel<32, 64, 4, false>;
+    const cudaError_t attr = set_max_dynamic_smem((const void*)kern, Cfg::SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(kern, dim3(ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st, mQK, mQK, mV,
+                      mDO, a);
+  }
+  using Cfg = FusedCfg<32, 64, 4, true>;
+  auto kern = attn_bwd_fused_kernel<32, 64, 4, true>;
   const cudaError_t attr = set_max_dynamic_smem((const void*)kern, Cfg::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
-  const int ctas = std::min(device_sm_count(), a.BH);
-  return launch_pdl(kern, dim3(ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st, mQK, mQK, mV,
-                    mDO, a);
+  return launch_pdl(kern, dim3(ctas), dim3(Cfg::kThreads), Cfg::SMEM_BYTES, st, mQK, mQK, mV, mDO,
+                    a);
 }
 
 }  // namespace psa

@@ -60,11 +60,13 @@ extern "C" psa_status_t psa_attention_bwd_noalloc(const void* qkv_nchw, const vo
   void* scratch = nullptr;
   psa_status_t e = delta_scratch(&scratch);
   if (e != PSA_OK) return e;
-  // Where the two-kernel backward runs (key_dim 64, or N > 512), the dQ kernel
-  // writes every delta value of this call before the dK/dV kernel reads it, so
-  // nothing an earlier call left in the array needs clearing; the one-kernel
-  // backward (key_dim 32, N <= 512) keeps delta on chip and does not touch the
-  // array, so only two-kernel calls can race on it.
+  // The array is psa_attention_bwd's workspace.  The two-kernel backward's dQ
+  // kernel writes every delta value of this call before the dK/dV kernel reads
+  // it; the one-kernel backward beyond 512 positions (chosen when its dQ
+  // accumulator fits) stores each accumulator row at the first key tile before it
+  // reads it at the next; up to 512 positions nothing touches the array.  So
+  // nothing an earlier call left needs clearing, and only calls that use the
+  // array can race on it.
   return psa_attention_bwd(qkv_nchw, out_nchw, dout_nchw, lse, dvres_nchw, dqkv_nchw, scratch,
                            kMaxDeltaFloats * sizeof(float), shape, scale, stream);
 }
