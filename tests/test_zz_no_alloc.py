@@ -1,8 +1,8 @@
 """psa_attention_bwd_noalloc: the fused PSA backward for callers that cannot
 allocate device memory when they run it (a plugin whose host framework owns every
 device allocation, or a latency-critical loop where cudaMalloc / cudaFree would
-synchronise the device).  Its delta scratch is a fixed array inside the library,
-so the caller passes only inputs and outputs.
+synchronise the device).  Its workspace is a fixed array inside the library, so
+the caller passes only inputs and outputs.
 
 The backward uses that array as its workspace: for delta in its two-kernel form
 (key_dim 64 below), and as the dQ accumulator of its one-kernel form between 512

@@ -137,6 +137,21 @@ bool map_nchw(CUtensorMap* m, const void* base, long long rows, int N, int box_r
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over the 2-D [rows, N] view of an NCHW output for TMA stores of
+// whole tiles: box {128 positions, box_rows channel rows}, no swizzle (the
+// staging tile is plain row-major).
+bool map_nchw_store(CUtensorMap* m, void* base, long long rows, int N, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor maps of the QKV convolution: w [cout, cin] (box {64, 128}) and x viewed as
 // 3-D (N, cin, B) (box {64, 64, 1}); positions and channels past the ends read as 0.
 bool map_conv(CUtensorMap* mw, CUtensorMap* mx, const void* w, const void* x, int B, int cin,
@@ -419,9 +434,16 @@ psa_status_t fused_fwd(const void* qkv, void* out, float* lse, void* v_nchw, voi
     a.lse = lse;
     e = from_cuda(psa::launch_simt_fwd(a, true, s.dtype == PSA_DTYPE_BF16, KD, st));
   } else {
-    CUtensorMap mqk, mv;
-    const long long rows = (long long)s.B * nh * 4 * KD;
+    CUtensorMap mqk, mv, mout, mvres;
+    const long long rows = (long long)s.B * nh * 4 * KD, orows = (long long)s.B * nh * 2 * KD;
     if (!map_nchw(&mqk, qkv, rows, N, KD) || !map_nchw(&mv, qkv, rows, N, 2 * KD))
+      return PSA_ERR_CUDA;
+    // Out and the extracted V are written by TMA stores: Out from the staged tile,
+    // V straight from the K/V stage (same box and swizzle as the V load)
+    mout = mv;
+    mvres = mv;
+    if ((out && !map_nchw_store(&mout, out, orows, N, 2 * KD)) ||
+        (v_nchw && !map_nchw(&mvres, v_nchw, orows, N, 2 * KD)))
       return PSA_ERR_CUDA;
     FwdArgs a{};
     a.N = N;
@@ -436,7 +458,7 @@ psa_status_t fused_fwd(const void* qkv, void* out, float* lse, void* v_nchw, voi
     a.vres = static_cast<__nv_bfloat16*>(v_nchw);  // PsaExtractV fused into the forward
     a.out_res = static_cast<__nv_bfloat16*>(out_res);
     a.qkv = static_cast<const __nv_bfloat16*>(qkv);
-    return from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, a, KD, st));
+    return from_cuda(psa::launch_psa_fwd_bf16(mqk, mv, mout, mvres, a, KD, st));
   }
   if (e != PSA_OK || !v_nchw) return e;
   return from_cuda(psa::launch_extract_v(qkv, v_nchw, s.B, nh, KD, N, elem_bytes(s.dtype), st));

@@ -27,8 +27,12 @@ struct FwdArgs {
 cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
                                 const CUtensorMap& mV, const FwdArgs& a, int d,
                                 cudaStream_t st);
-// NCHW: 2-D maps over [B*qkv_ch, N] with boxes {64, KD} (Q, K) and {64, 2*KD} (V).
+// NCHW: 2-D maps over [B*qkv_ch, N] with boxes {64, KD} (Q, K) and {64, 2*KD} (V);
+// mOut over [B*out_ch, N] with box {128, 2*KD}, no swizzle (TMA store of a.out);
+// mVres over [B*vres_ch, N] like mV (TMA store of a.vres).  A map whose pointer
+// is null is never used.
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
+                                const CUtensorMap& mOut, const CUtensorMap& mVres,
                                 const FwdArgs& a, int KD, cudaStream_t st);
 
 // CUDA-core path (attn_simt.cu): fp32 or bf16 storage, any N, fp32 arithmetic.

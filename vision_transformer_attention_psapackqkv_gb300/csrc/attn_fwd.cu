@@ -20,6 +20,8 @@
 //   warp P + 2         P.V issuer (one thread): O += P_k V_k -> TMEM (DV
 //                      columns), P_k read from tensor memory (A operand;
 //                      double-buffered)
+//   warp P + 3         store warp (NCHW): TMA stores of each finished O tile and
+//                      bulk copies of its LSE, from a shared-memory staging tile
 // The bf16 kernels run persistent grids; with one slot per CTA two CTAs share
 // an SM (and its tensor core), which interleaves their softmax and MMA phases.
 // Split rows (kSplit, short sequences): warps 0-3 and 4-7 both cover the 128 rows,
@@ -35,11 +37,15 @@
 // shared memory; O is rescaled in TMEM only when a row
 // max grows by more than 2^8 (exact either way, since O and the running sum
 // share the stale max).  Epilogue: O / l in the output layout and the LSE.
+// The row threads issue no global store in the NCHW layout: an mbarrier arrive
+// has release semantics, so every hand-off after a global store would wait for
+// that store to be acknowledged (measured ~0.7-1k cycles per step); they stage O
+// and the LSE in shared memory for the store warp instead.
 // Layouts: kNCHW = false reads [BH, N, D] planes (Q, K K-major; V MN-major);
 // kNCHW = true reads the QKV conv output [B, nh*4*KD, N] directly (Q, K
 // MN-major; V K-major), which fuses PsaPackQkv, both V-half runs (one softmax,
-// DV = 2*KD), PsaMergeAttn, and optionally PsaExtractV (the slot whose query tile
-// index equals the key tile index copies that V tile out of shared memory).
+// DV = 2*KD), PsaMergeAttn, and optionally PsaExtractV (for the slot whose query
+// tile covers a key tile, the S issuer TMA-stores that V tile from its K/V stage).
 //
 // fp32 storage and maps whose rows TMA cannot address run on CUDA cores
 // (attn_simt.cu).
@@ -69,10 +75,11 @@ struct FwdCfg {
   static constexpr int HC = BN / H;         // S columns per softmax thread
   static constexpr int kRowThreads = 128 * H;  // softmax threads of a slot
   static constexpr int kSoftmaxWarps = 4 * NWG * H;
-  // control warps: TMA producer, S issuer (TMEM owner), P.V issuer
+  // control warps: TMA producer, S issuer (TMEM owner), P.V issuer, and the store
+  // warp that writes the staged output tiles (NCHW) with TMA
   static constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
-  static constexpr int kPvWarp = kSoftmaxWarps + 2;
-  static constexpr int kThreads = 32 * kSoftmaxWarps + 96;
+  static constexpr int kPvWarp = kSoftmaxWarps + 2, kStoreWarp = kSoftmaxWarps + 3;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 128;
   static constexpr uint32_t Q_BYTES = BM * DQK * 2;
   static constexpr uint32_t K_BYTES = BN * DQK * 2;
   static constexpr uint32_t V_BYTES = BN * DV * 2;
@@ -82,7 +89,12 @@ struct FwdCfg {
   static constexpr uint32_t SL_V = SL_K + STAGES * K_BYTES;
   // split rows: per tile parity, (max, sum) of both halves of every row
   static constexpr uint32_t SL_ML = SL_V + STAGES * V_BYTES;
-  static constexpr uint32_t SL_BYTES = SL_ML + (kSplit ? 2 * 2 * BM * 8 : 0);
+  // NCHW: the finished O tile (DV channel rows of BM positions, bf16, unswizzled)
+  // and its BM LSE values, staged for the store warp's TMA stores
+  static constexpr uint32_t SL_OUT = SL_ML + (kSplit ? 2 * 2 * BM * 8 : 0);
+  static constexpr uint32_t OUT_BYTES = kNCHW ? DV * BM * 2 : 0;
+  static constexpr uint32_t SL_LSE = SL_OUT + OUT_BYTES;
+  static constexpr uint32_t SL_BYTES = SL_LSE + (kNCHW ? 1024 : 0);
   static constexpr uint32_t OFF_BAR = NWG * SL_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
   // tensor memory per slot w: S (BN columns) at TM_SLOT * w, then H O accumulators
@@ -92,7 +104,9 @@ struct FwdCfg {
   static constexpr uint32_t TM_P = BN + H * DV;
   static constexpr uint32_t TM_SLOT = (TM_P + BN <= 128) ? 128 : 256;
   static_assert(TM_P + BN <= 256, "tensor memory per slot");
-  static_assert(SL_ML % 1024 == 0, "1024-byte aligned (max, sum) area");
+  static_assert(SL_ML % 1024 == 0 && SL_OUT % 1024 == 0 && SL_LSE % 1024 == 0,
+                "1024-byte aligned (max, sum) and staging areas");
+  static_assert(BM * 4 <= 1024, "LSE staging");
   static constexpr uint32_t TMEM_COLS = NWG * TM_SLOT < 32 ? 32 : NWG * TM_SLOT;
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(DQK % 16 == 0 && DV % 32 == 0 && DV <= 128, "tile shape");
@@ -104,6 +118,7 @@ struct SlotBars {
   uint64_t q_full[2], q_empty[2], kv_full[4], kv_empty[4];
   uint64_t s_full, s_free, p_full[2], pv_done[2], o_free;  // P / P.V per P buffer
   uint64_t ml_ready;  // split rows: both halves' (max, sum) of the tile are in shared memory
+  uint64_t out_full, out_free;  // NCHW: the staged O / LSE tile is written / stored
 };
 
 // Loads this thread's NC-column S row from TMEM into registers with a single
@@ -147,8 +162,12 @@ __device__ __forceinline__ float softmax_row(uint32_t (&s)[NC], int valid, float
   // instructions: half the issue slots of scalar FMA / add)
   const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m_run, -m_run);
   float2 l01 = make_float2(0.f, 0.f), l23 = make_float2(0.f, 0.f);
+  // a partial tile skips the 16-column blocks beyond its last valid column (the
+  // P.V product reads no P of those blocks); the test is uniform across a warp
+  const int vend = kFull ? NC : ((valid + 15) & ~15);
 #pragma unroll
   for (int c = 0; c < NC; c += 4) {
+    if (!kFull && c >= vend) break;
     const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
                                   sl2x2, nm2);
     const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])),
@@ -187,11 +206,45 @@ __device__ __forceinline__ int slot_tiles(int slot, int nslots, int T) {
   return slot < T ? (T - slot + nslots - 1) / nslots : 0;
 }
 
+// Writes channels [ch, ch + n) of O's row r (query q; live: q < N) of head bh.
+// NCHW: into the staging tile (channel rows of 128 positions, bf16) when Out is
+// wanted, and Out + V (V read at the query position) straight to out_res when the
+// residual output is wanted; raw layout: 16-byte stores of the row.
+template <int DQK, int DV, bool kNCHW, int n>
+__device__ __forceinline__ void emit_row(const FwdArgs& args, int N, uint32_t stg, int bh, int r,
+                                         int q, bool live, int ch, const float (&o)[n]) {
+  if (kNCHW) {
+    if (args.out) {
+#pragma unroll
+      for (int e = 0; e < n; ++e) st_shared_bf16(stg + ((ch + e) * 128 + r) * 2, o[e]);
+    }
+    if (args.out_res && live) {
+      const long long orow =
+          ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + ch) * N + q;
+      const __nv_bfloat16* vsrc =
+          args.qkv + ((long long)(bh / args.nh) * args.qkv_ch + (bh % args.nh) * 4 * DQK + 2 * DQK + ch) *
+                         N + q;
+#pragma unroll
+      for (int e = 0; e < n; ++e)
+        args.out_res[orow + (long long)e * N] =
+            __float2bfloat16_rn(o[e] + __bfloat162float(vsrc[(long long)e * N]));
+    }
+  } else if (live) {
+    uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + ch);
+#pragma unroll
+    for (int e = 0; e < n; e += 8)
+      dst[e / 8] = make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
+                              pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
+  }
+}
+
 template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
-__global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 2 : 1)
+__global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ? 2 : 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQK,
                        const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmOut,
+                       const __grid_constant__ CUtensorMap tmVres, const FwdArgs args) {
   using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -218,7 +271,9 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
       }
       for (int i = 0; i < C::STAGES; ++i) {
         mbar_init(&b.kv_full[i], 1);
-        mbar_init(&b.kv_empty[i], 2);  // K read by S, V by P.V: one commit each
+        // K read by S, V by P.V: one commit each; NCHW: and the S issuer's arrival
+        // once its PsaExtractV store has read the stage
+        mbar_init(&b.kv_empty[i], kNCHW ? 3 : 2);
       }
       mbar_init(&b.s_full, 1);
       mbar_init(&b.s_free, C::kRowThreads);
@@ -228,6 +283,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
       }
       mbar_init(&b.o_free, C::kRowThreads);
       mbar_init(&b.ml_ready, C::kRowThreads);
+      mbar_init(&b.out_full, C::kRowThreads);
+      mbar_init(&b.out_free, 1);
     }
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
@@ -371,6 +428,26 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
         mma_commit(&b.s_full);
         mma_commit(&b.kv_empty[k % C::STAGES]);
         if (j == nkv - 1) mma_commit(&b.q_empty[i % QBUF]);
+        if (kNCHW) {
+          // PsaExtractV: the slot whose query tile covers key tile j stores V tile j
+          // (already in shared memory for P.V) to the NCHW output with TMA; the
+          // stage is released once the store has read it
+          if (args.vres != nullptr) {
+            int bh, qt;
+            tile_coords(blockIdx.x * NWG + w + i * nslots, args.BH, nfull, bh, qt);
+            if ((j * C::BN) / C::BM == qt) {
+              const unsigned char* vt =
+                  smem + w * C::SL_BYTES + C::SL_V + (k % C::STAGES) * C::V_BYTES;
+              const int vrow = (bh / args.nh) * args.vres_ch + (bh % args.nh) * DV;
+#pragma unroll
+              for (int bx = 0; bx < C::BN / 64; ++bx)
+                tma_store_2d(&tmVres, vt + bx * (DV * 128), j * C::BN + 64 * bx, vrow);
+              bulk_commit();
+              bulk_wait_read_all();
+            }
+          }
+          mbar_arrive(&b.kv_empty[k % C::STAGES]);
+        }
         return true;
       };
       auto issue_pv = [&](int w, int i, int j) -> bool {
@@ -410,6 +487,40 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
       uint64_t* done = &mma_done[s_role ? 0 : 1];
       mma_commit(done);
       drain_wait(done, 0);  // every MMA retired before TMEM is released
+      if (kNCHW && s_role) bulk_wait_all();
+    }
+  } else if (warp == C::kStoreWarp) {
+    // ------------------------------------------------------------ store warp
+    // NCHW: once the row threads have staged a finished tile (O rows of BM
+    // positions, LSE), one TMA store writes O (positions >= N are clipped) and a
+    // bulk copy the LSE of the live rows; the staging area is handed back once the
+    // copies have read it.  Row threads thus issue no global stores.
+    if (kNCHW && lane == 0) {
+      tma_prefetch_desc(&tmOut);
+      bool ok = true;
+      for (int i = 0; ok && i < max_tiles; ++i)
+        for (int w = 0; ok && w < NWG; ++w) {
+          if (i >= ntiles[w]) continue;
+          SlotBars& b = bars[w];
+          if (!mbar_wait(&b.out_full, i & 1, abort)) {
+            ok = false;
+            break;
+          }
+          int bh, qt;
+          tile_coords(blockIdx.x * NWG + w + i * nslots, args.BH, nfull, bh, qt);
+          const int q0 = qt * C::BM;
+          const unsigned char* sl = smem + w * C::SL_BYTES;
+          if (args.out)
+            tma_store_2d(&tmOut, sl + C::SL_OUT, q0,
+                         (bh / args.nh) * args.out_ch + (bh % args.nh) * DV);
+          if (args.lse)  // N % 8 == 0: a multiple of 32 bytes
+            bulk_store(args.lse + (long long)bh * N + q0, sl + C::SL_LSE,
+                       (uint32_t)min(C::BM, N - q0) * 4u);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&b.out_free);
+        }
+      bulk_wait_all();
     }
   }
   } else {
@@ -418,7 +529,6 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
     const int h = kSplit ? warp >> 2 : 0;  // key half of every tile this thread owns
     const int wq = warp & 3;               // TMEM lane quadrant
     const int r = wq * 32 + lane;          // query row within the tile = TMEM lane
-    const int tid = h * 128 + r;           // softmax thread within the slot
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     // S, and the O accumulator of this thread's key half
     const uint32_t tS = tmem + w * C::TM_SLOT, tO = tS + C::TM_O + h * DV;
@@ -427,6 +537,84 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
     const float sl2 = args.scale_log2;
     const int my_tiles = slot_tiles(blockIdx.x * NWG + w, nslots, T);
     bool ok = true;
+    // Epilogue of this slot's tile i (m_run / l_run: the running max and sum of
+    // this thread's row): O / l and the LSE in natural-log units.  NCHW: the row
+    // threads stage both in shared memory for the store warp (no global store on
+    // their path); raw layout: 16-byte stores of the thread's own row.  The next
+    // tile's first P.V waits for o_free, arrived once O has been read.  (Running
+    // it after the next tile's first P hand-off instead measured slower: the
+    // next tile's state stays live across it and spills.)
+    auto finish_tile = [&](int i, float m_run, float l_run) -> bool {
+      int bh, qt;
+      tile_coords(blockIdx.x * NWG + w + i * nslots, args.BH, nfull, bh, qt);
+      const int q0 = qt * C::BM, q = q0 + r;
+      const bool active = wq * 32 < N - q0, live = q < N;
+      const int klast = i * nkv + nkv - 1;
+      if (!mbar_wait(&b.pv_done[klast & 1], (klast >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      // NCHW: the staging area is free once the previous tile's stores have read it
+      if (kNCHW && i > 0 && !mbar_wait(&b.out_free, (i - 1) & 1, abort)) return false;
+      float lse = 0.f;
+      if (kSplit) {
+        // both halves' (max, sum) of the row, then this thread writes channels
+        // [h * DV/2, (h + 1) * DV/2) of O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l
+        float* ml = reinterpret_cast<float*>(smem + w * C::SL_BYTES + C::SL_ML) + (i & 1) * 512;
+        ml[h * 256 + 2 * r] = m_run;
+        ml[h * 256 + 2 * r + 1] = l_run;
+        mbar_arrive(&b.ml_ready);
+        if (!mbar_wait(&b.ml_ready, i & 1, abort)) return false;
+        const float m0 = ml[2 * r], l0 = ml[2 * r + 1];
+        const float m1 = ml[256 + 2 * r], l1 = ml[256 + 2 * r + 1];
+        // a half without any valid key (N <= 32) has l = 0 and an unwritten accumulator
+        const float mx = l1 > 0.f ? fmaxf(m0, m1) : m0;
+        const float f0 = fast_exp2(m0 - mx), f1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
+        const float l = l0 * f0 + l1 * f1;
+        const float c0s = f0 / l, c1s = f1 / l;
+        if (active) {
+#pragma unroll 1
+          for (int c = 0; c < DV / 2; c += 16) {
+            const int ch = h * (DV / 2) + c;
+            uint32_t a0[16], a1[16];
+            tmem_load16_async(tS + C::TM_O + lane_base + ch, a0);
+            tmem_load16_async(tS + C::TM_O + DV + lane_base + ch, a1);
+            tmem_wait_ld();
+            tmem_pin(a0);
+            tmem_pin(a1);
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[e] = l1 > 0.f ? __uint_as_float(a0[e]) * c0s + __uint_as_float(a1[e]) * c1s
+                              : __uint_as_float(a0[e]) * c0s;
+            emit_row<DQK, DV, kNCHW>(args, N, sl + C::SL_OUT, bh, r, q, live, ch, o);
+          }
+        }
+        lse = (mx + log2f(l)) * kLn2;
+      } else if (active) {
+        const float inv_l = 1.f / l_run;
+#pragma unroll 1
+        for (int c = 0; c < DV; c += 32) {
+          float o[32];
+          tmem_load32(tO + lane_base + c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= inv_l;
+          emit_row<DQK, DV, kNCHW>(args, N, sl + C::SL_OUT, bh, r, q, live, c, o);
+        }
+        lse = (m_run + log2f(l_run)) * kLn2;
+      }
+      tc_fence_before();
+      mbar_arrive(&b.o_free);
+      if (h == 0 && active && args.lse) {
+        if (kNCHW)
+          st_shared_f32(sl + C::SL_LSE + r * 4, lse);
+        else if (live)
+          args.lse[(long long)bh * N + q] = lse;
+      }
+      if (kNCHW) {
+        fence_proxy_async_smem();
+        mbar_arrive(&b.out_full);
+      }
+      return true;
+    };
     for (int i = 0; ok && i < my_tiles; ++i) {
       const int t = blockIdx.x * NWG + w + i * nslots;
       int bh, qt;
@@ -445,34 +633,6 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
           break;
         }
         tc_fence_after();
-        if (kNCHW && args.vres != nullptr && (j * C::BN) / C::BM == qt) {
-          // PsaExtractV: the slot whose query tile covers key tile j copies V tile j
-          // (rows = DV channels, BN/64 boxes of 64 positions) from shared memory to
-          // the NCHW output.  The stage stays resident until this slot's P_k is
-          // handed over.
-          if (!mbar_wait(&b.kv_full[k % C::STAGES], (k / C::STAGES) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          constexpr int kBoxes = C::BN / 64;
-          const uint32_t vb = sl + C::SL_V + (k % C::STAGES) * C::V_BYTES;
-          for (int e = tid; e < DV * kBoxes; e += C::kRowThreads) {
-            const int ch = e / kBoxes, box = e % kBoxes;
-            const int pos0 = j * C::BN + box * 64;
-            __nv_bfloat16* dst = args.vres +
-                ((long long)(bh / args.nh) * args.vres_ch + (bh % args.nh) * DV + ch) * N + pos0;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              if (pos0 + c8 * 8 < N) {
-                uint4 v;
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                             : "r"(vb + box * (DV * 128) + swizzled_offset(ch, c8, 128)));
-                *reinterpret_cast<uint4*>(dst + c8 * 8) = v;
-              }
-            }
-          }
-        }
         // this thread's part of the S row goes to registers at once, so the S buffer
         // is handed back to the MMA warp (which starts S_{k+1}) before the
         // exponentials
@@ -519,118 +679,7 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
         mbar_arrive(&b.p_full[k & 1]);
       }
       if (!ok) break;
-      // epilogue: O / l in the output layout, LSE in natural-log units
-      const int klast = i * nkv + nkv - 1;
-      if (!mbar_wait(&b.pv_done[klast & 1], (klast >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (kSplit) {
-        // both halves' (max, sum) of the row, then this thread writes channels
-        // [h * DV/2, (h + 1) * DV/2) of O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l
-        float* ml = reinterpret_cast<float*>(smem + w * C::SL_BYTES + C::SL_ML) + (i & 1) * 512;
-        ml[h * 256 + 2 * r] = m_run;
-        ml[h * 256 + 2 * r + 1] = l_run;
-        mbar_arrive(&b.ml_ready);
-        if (!mbar_wait(&b.ml_ready, i & 1, abort)) {
-          ok = false;
-          break;
-        }
-        const float m0 = ml[2 * r], l0 = ml[2 * r + 1];
-        const float m1 = ml[256 + 2 * r], l1 = ml[256 + 2 * r + 1];
-        // a half without any valid key (N <= 32) has l = 0 and an unwritten accumulator
-        const float mx = l1 > 0.f ? fmaxf(m0, m1) : m0;
-        const float f0 = fast_exp2(m0 - mx), f1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
-        const float l = l0 * f0 + l1 * f1;
-        const float c0s = f0 / l, c1s = f1 / l;
-        if (active) {
-          const int q = q0 + r;
-          const bool live = q < N;
-#pragma unroll 1
-          for (int c = 0; c < DV / 2; c += 16) {
-            const int ch = h * (DV / 2) + c;
-            uint32_t a0[16], a1[16];
-            tmem_load16_async(tS + C::TM_O + lane_base + ch, a0);
-            tmem_load16_async(tS + C::TM_O + DV + lane_base + ch, a1);
-            tmem_wait_ld();
-            tmem_pin(a0);
-            tmem_pin(a1);
-            float o[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              o[e] = l1 > 0.f ? __uint_as_float(a0[e]) * c0s + __uint_as_float(a1[e]) * c1s
-                              : __uint_as_float(a0[e]) * c0s;
-            if (live) {
-              if (kNCHW) {
-                const long long orow =
-                    ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + ch) * N + q;
-                if (args.out) {
-#pragma unroll
-                  for (int e = 0; e < 16; ++e)
-                    args.out[orow + (long long)e * N] = __float2bfloat16_rn(o[e]);
-                }
-                if (args.out_res) {
-                  const __nv_bfloat16* vsrc = args.qkv + ((long long)(bh / args.nh) * args.qkv_ch +
-                                                          (bh % args.nh) * 4 * DQK + 2 * DQK + ch) * N + q;
-#pragma unroll
-                  for (int e = 0; e < 16; ++e)
-                    args.out_res[orow + (long long)e * N] =
-                        __float2bfloat16_rn(o[e] + __bfloat162float(vsrc[(long long)e * N]));
-                }
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + ch);
-#pragma unroll
-                for (int e = 0; e < 16; e += 8)
-                  dst[e / 8] = make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
-                                          pack_bf16x2(o[e + 4], o[e + 5]),
-                                          pack_bf16x2(o[e + 6], o[e + 7]));
-              }
-            }
-          }
-          if (h == 0 && live && args.lse)
-            args.lse[(long long)bh * N + q] = (mx + log2f(l)) * kLn2;
-        }
-      } else if (active) {
-        const float inv_l = 1.f / l_run;
-        const int q = q0 + r;
-        const bool live = q < N;
-#pragma unroll
-        for (int c = 0; c < DV; c += 32) {
-          float o[32];
-          tmem_load32(tO + lane_base + c, o);
-          if (live) {
-            if (kNCHW) {
-              const long long orow =
-                  ((long long)(bh / args.nh) * args.out_ch + (bh % args.nh) * DV + c) * N + q;
-              if (args.out) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  args.out[orow + (long long)e * N] = __float2bfloat16_rn(o[e] * inv_l);
-              }
-              if (args.out_res) {
-                const __nv_bfloat16* vsrc = args.qkv + ((long long)(bh / args.nh) * args.qkv_ch +
-                                                        (bh % args.nh) * 4 * DQK + 2 * DQK + c) * N + q;
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  args.out_res[orow + (long long)e * N] =
-                      __float2bfloat16_rn(o[e] * inv_l + __bfloat162float(vsrc[(long long)e * N]));
-              }
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(args.out + ((long long)bh * N + q) * DV + c);
-#pragma unroll
-              for (int e = 0; e < 32; e += 8)
-                dst[e / 8] = make_uint4(pack_bf16x2(o[e] * inv_l, o[e + 1] * inv_l),
-                                        pack_bf16x2(o[e + 2] * inv_l, o[e + 3] * inv_l),
-                                        pack_bf16x2(o[e + 4] * inv_l, o[e + 5] * inv_l),
-                                        pack_bf16x2(o[e + 6] * inv_l, o[e + 7] * inv_l));
-            }
-          }
-        }
-        if (live && args.lse) args.lse[(long long)bh * N + q] = (m_run + log2f(l_run)) * kLn2;
-      }
-      tc_fence_before();
-      mbar_arrive(&b.o_free);
+      if (!finish_tile(i, m_run, l_run)) break;
     }
   }
 
@@ -644,7 +693,8 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 96, NWG == 1 ? 
 
 template <int DQK, int DV, bool kNCHW, int NWG, int QBUF, int ST, bool kSplit>
 cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUtensorMap& mV,
-                      const FwdArgs& a, cudaStream_t st) {
+                      const CUtensorMap& mOut, const CUtensorMap& mVres, const FwdArgs& a,
+                      cudaStream_t st) {
   using C = FwdCfg<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   auto kern = attn_fwd_tc_kernel<DQK, DV, kNCHW, NWG, QBUF, ST, kSplit>;
   const cudaError_t attr = set_max_dynamic_smem((const void*)kern, C::SMEM_BYTES);
@@ -654,7 +704,7 @@ cudaError_t launch_tc(const CUtensorMap& mQK, const CUtensorMap& mK, const CUten
   const long long per_sm = NWG == 1 ? 2 : 1;
   const long long ctas = std::min<long long>(per_sm * device_sm_count(), (T + NWG - 1) / NWG);
   return launch_pdl(kern, dim3((unsigned)ctas), dim3(C::kThreads), C::SMEM_BYTES, st, mQK, mK,
-                    mV, a);
+                    mV, mOut, mVres, a);
 }
 
 }  // namespace
@@ -666,18 +716,21 @@ cudaError_t launch_fa2_fwd_bf16(const CUtensorMap& mQ, const CUtensorMap& mK,
   // per SM, each within half of the SM's shared memory and tensor memory
   // (split rows measured slower on long sequences: the hand-off chain between the
   // row threads and the MMA warp, not the per-row exponentials, sets their pace)
-  if (d == 32) return launch_tc<32, 32, false, 1, 2, 4, false>(mQ, mK, mV, a, st);
-  return launch_tc<64, 64, false, 1, 1, 3, false>(mQ, mK, mV, a, st);
+  // (the raw layout stores O from the row threads: the output maps are unused)
+  if (d == 32) return launch_tc<32, 32, false, 1, 2, 4, false>(mQ, mK, mV, mV, mV, a, st);
+  return launch_tc<64, 64, false, 1, 1, 3, false>(mQ, mK, mV, mV, mV, a, st);
 }
 
 cudaError_t launch_psa_fwd_bf16(const CUtensorMap& mQK, const CUtensorMap& mV,
+                                const CUtensorMap& mOut, const CUtensorMap& mVres,
                                 const FwdArgs& a, int KD, cudaStream_t st) {
   // split rows for the short sequences of vision feature maps (N = 400: 41.7 against
   // 42.7 us), one thread per row beyond (N = 1600: 267 against 291 us)
-  if (KD == 32 && a.N <= 512) return launch_tc<32, 64, true, 1, 2, 4, true>(mQK, mQK, mV, a, st);
-  if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4, false>(mQK, mQK, mV, a, st);
+  if (KD == 32 && a.N <= 512)
+    return launch_tc<32, 64, true, 1, 2, 4, true>(mQK, mQK, mV, mOut, mVres, a, st);
+  if (KD == 32) return launch_tc<32, 64, true, 1, 2, 4, false>(mQK, mQK, mV, mOut, mVres, a, st);
   // DV = 128: two accumulators would not leave room for a second CTA's tensor memory
-  return launch_tc<64, 128, true, 1, 1, 2, false>(mQK, mQK, mV, a, st);
+  return launch_tc<64, 128, true, 1, 1, 2, false>(mQK, mQK, mV, mOut, mVres, a, st);
 }
 
 }  // namespace psa
