@@ -143,14 +143,25 @@ template <bool kFull, int NC>
 __device__ __forceinline__ float softmax_row(uint32_t (&s)[NC], int valid, float sl2, bool first,
                                              float& m_run, float& l_run) {
   float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+  if (kFull) {
+    // two new columns per three-input max, four independent chains
 #pragma unroll
-  for (int c = 0; c < NC; c += 4) {
-    if (kFull || c < valid) m0 = fmaxf(m0, __uint_as_float(s[c]));
-    if (kFull || c + 1 < valid) m1 = fmaxf(m1, __uint_as_float(s[c + 1]));
-    if (kFull || c + 2 < valid) m2 = fmaxf(m2, __uint_as_float(s[c + 2]));
-    if (kFull || c + 3 < valid) m3 = fmaxf(m3, __uint_as_float(s[c + 3]));
+    for (int c = 0; c < NC; c += 8) {
+      m0 = fmax3(m0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+      m1 = fmax3(m1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+      m2 = fmax3(m2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+      m3 = fmax3(m3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; c += 4) {
+      if (c < valid) m0 = fmaxf(m0, __uint_as_float(s[c]));
+      if (c + 1 < valid) m1 = fmaxf(m1, __uint_as_float(s[c + 1]));
+      if (c + 2 < valid) m2 = fmaxf(m2, __uint_as_float(s[c + 2]));
+      if (c + 3 < valid) m3 = fmaxf(m3, __uint_as_float(s[c + 3]));
+    }
   }
-  const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
+  const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * sl2;
   float alpha = 1.f;
   if (first) {
     m_run = mx;
