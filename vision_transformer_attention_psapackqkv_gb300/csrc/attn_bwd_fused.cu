@@ -231,12 +231,15 @@ __global__ void __launch_bounds__(896, 1)
     bool ok = true;
     int kvc = 0, qc = 0;
     constexpr int kPer = C::CHUNK / 32;
+    // raw lse values: nothing consumes them until they are written to shared
+    // memory, so the loads stay in flight while the producer goes on issuing
+    // copies (scaling them at load time would stall it on the loads)
     float nl[kPer];
     auto load_chunk = [&](int bh, int c0) {
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const int q = c0 + lane + 32 * i;
-        nl[i] = q < N ? -args.lse[(long long)bh * N + q] * kLog2e : -INFINITY;
+        nl[i] = q < N ? args.lse[(long long)bh * N + q] : 0.f;
       }
     };
     if (nunits > 0) load_chunk(head_of(0), 0);
@@ -250,7 +253,8 @@ __global__ void __launch_bounds__(896, 1)
       for (int c0 = 0; c0 < C::MAXN; c0 += C::CHUNK) {
         if (c0 > 0) load_chunk(bh, c0);
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) hst[c0 + lane + 32 * i] = nl[i];
+        for (int i = 0; i < kPer; ++i)
+          hst[c0 + lane + 32 * i] = c0 + lane + 32 * i < N ? -nl[i] * kLog2e : -INFINITY;
       }
       mbar_arrive(&b.hs_full[u & 1]);
       if (u + 1 < nunits) load_chunk(head_of(u + 1), 0);
