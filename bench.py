@@ -518,12 +518,14 @@ def _time_graph(torch, fn, iters, warmup):
     with torch.cuda.graph(g, stream=s):
         for i in range(iters):
             fn(i)
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    g.replay()
-    e1.record(s)
+    # replay() launches on the current stream (not the capture stream): time there
+    with torch.cuda.stream(s):
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.replay()
+        e1.record(s)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters * 1e-3
 
