@@ -92,17 +92,34 @@ __global__ void __launch_bounds__(kThreads) rows_to_channels_kernel(TransposeArg
 // ---------------------------------------------------------------- 16-byte vectors
 // The same two transposes for bf16 when every channel row and every position row
 // starts on a 16-byte boundary (N % 8 == 0 and KD % 8 == 0): each CTA moves a tile
-// of KD channels x up to 512 positions of one (batch, head, plane); global memory
-// is read and written only in 16-byte vectors (8 elements), four per thread in
-// flight at a time, and shared memory holds the tile as 16-byte chunks (chunk
-// (d, c) = channel d, positions 8c .. 8c+7), row-major with the chunk index XOR-ed
-// with (d / 8) % 8.  The element-wise side of the transpose (8 channels of one
-// position per thread) then reads 8 different chunks per instruction across a warp
-// without bank conflicts, and the chunk-wise side stays conflict-free.
+// of KD channels x up to 512 positions of one (batch, head, plane); global and
+// shared memory are only read and written in 16-byte vectors (8 elements), and
+// shared memory holds the tile as 16-byte chunks (chunk (d, c) = channel d,
+// positions 8c .. 8c+7), row-major with the chunk index XOR-ed with (d / 8) % 8.
+// The position-row side works on 8 x 8 blocks (8 channels x 8 positions per
+// thread, transposed in registers with byte permutes): its warp reads or writes
+// the chunks (8g + i, c) of 8 c and 4 g per instruction without bank conflicts,
+// and in global memory the threads of one c cover whole position rows side by
+// side.  The channel-row side moves chunks along the NCHW rows, four per thread
+// in flight.
 constexpr int kVecTileN = 512;
 constexpr int kVecChunks = kVecTileN / 8;  // 16-byte chunks per channel row of the tile
 
 __device__ __forceinline__ int vec_chunk(int d, int c) { return d * kVecChunks + (c ^ ((d >> 3) & 7)); }
+
+// Row j of the 8 x 8 transpose of 16-bit elements held as eight 16-byte vectors:
+// in[i] holds elements (i, 0..7) (two per 32-bit word, the lower index in the low
+// half); the result holds elements (0..7, j).  One byte permute per word: 0x5410
+// takes the low halves of its two words, 0x7632 the high halves.
+__device__ __forceinline__ uint4 transpose8x8_row(const uint4 (&in)[8], int j) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(in);  // w[4 i + k]
+  const int k = j >> 1;
+  const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+  return make_uint4(__byte_perm(w[0 * 4 + k], w[1 * 4 + k], sel),
+                    __byte_perm(w[2 * 4 + k], w[3 * 4 + k], sel),
+                    __byte_perm(w[4 * 4 + k], w[5 * 4 + k], sel),
+                    __byte_perm(w[6 * 4 + k], w[7 * 4 + k], sel));
+}
 
 // Plane pointer s of four without a local-memory copy of the array.
 template <typename P>
@@ -110,10 +127,9 @@ __device__ __forceinline__ P plane_ptr(const P (&p)[4], int s) {
   return s == 0 ? p[0] : s == 1 ? p[1] : s == 2 ? p[2] : p[3];
 }
 
-__global__ void __launch_bounds__(kThreads) channels_to_rows_vec_kernel(const TransposeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const TransposeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* tile = reinterpret_cast<uint4*>(smem_raw);  // KD x kVecChunks chunks
-  const uint16_t* tile16 = reinterpret_cast<const uint16_t*>(smem_raw);
   const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
   const int unit = blockIdx.x / ntiles;
   const int s = unit % a.planes;
@@ -146,29 +162,26 @@ __global__ void __launch_bounds__(kThreads) channels_to_rows_vec_kernel(const Tr
     }
   }
   __syncthreads();
+  // one item = channels 8g .. 8g+7 x positions 8c .. 8c+7: eight chunk reads, a
+  // register transpose, eight position-row writes (the dvec threads of one c
+  // write whole position rows side by side)
   const int dvec = a.KD / 8;
   uint4* dst = reinterpret_cast<uint4*>(plane_ptr(a.rows_dst, s)) +
                ((long long)bhd * a.N + n0) * dvec;
-  const int nstore = nvalid * dvec;
-#pragma unroll 4
-  for (int idx = threadIdx.x; idx < nstore; idx += kThreads) {
-    const int n = idx / dvec, g = idx - n * dvec;
-    uint32_t w[4];
+  const int nitems = dvec * cvalid;
+  for (int idx = threadIdx.x; idx < nitems; idx += kThreads) {
+    const int c = idx / dvec, g = idx - c * dvec;
+    uint4 in[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int d0 = 8 * g + 2 * e;
-      const uint32_t lo = tile16[vec_chunk(d0, n >> 3) * 8 + (n & 7)];
-      const uint32_t hi = tile16[vec_chunk(d0 + 1, n >> 3) * 8 + (n & 7)];
-      w[e] = lo | (hi << 16);
-    }
-    dst[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 8; ++i) in[i] = tile[vec_chunk(8 * g + i, c)];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[(long long)(8 * c + j) * dvec + g] = transpose8x8_row(in, j);
   }
 }
 
-__global__ void __launch_bounds__(kThreads) rows_to_channels_vec_kernel(const TransposeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) rows_to_channels_vec_kernel(const TransposeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const uint4* tile = reinterpret_cast<const uint4*>(smem_raw);
-  uint16_t* tile16 = reinterpret_cast<uint16_t*>(smem_raw);
+  uint4* tile = reinterpret_cast<uint4*>(smem_raw);
   const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
   const int unit = blockIdx.x / ntiles;
   const int s = unit % a.planes;
@@ -180,28 +193,16 @@ __global__ void __launch_bounds__(kThreads) rows_to_channels_vec_kernel(const Tr
   const int dvec = a.KD / 8;
   const uint4* src = reinterpret_cast<const uint4*>(plane_ptr(a.rows_src, s)) +
                      ((long long)bhd * a.N + n0) * dvec;
-  const int nload = nvalid * dvec;
-  for (int i0 = threadIdx.x; i0 < nload; i0 += 4 * kThreads) {
-    uint4 v[4];
+  // one item = positions 8c .. 8c+7 x channels 8g .. 8g+7: eight position-row
+  // reads (eight in flight), a register transpose, eight chunk writes
+  const int nitems = dvec * cvalid;
+  for (int idx = threadIdx.x; idx < nitems; idx += kThreads) {
+    const int c = idx / dvec, g = idx - c * dvec;
+    uint4 in[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int idx = i0 + u * kThreads;
-      if (idx < nload) v[u] = __ldg(src + idx);
-    }
+    for (int j = 0; j < 8; ++j) in[j] = __ldg(src + (long long)(8 * c + j) * dvec + g);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int idx = i0 + u * kThreads;
-      if (idx < nload) {
-        const int n = idx / dvec, g = idx - n * dvec;
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int d0 = 8 * g + 2 * e;
-          tile16[vec_chunk(d0, n >> 3) * 8 + (n & 7)] = (uint16_t)(w[e] & 0xffffu);
-          tile16[vec_chunk(d0 + 1, n >> 3) * 8 + (n & 7)] = (uint16_t)(w[e] >> 16);
-        }
-      }
-    }
+    for (int i = 0; i < 8; ++i) tile[vec_chunk(8 * g + i, c)] = transpose8x8_row(in, i);
   }
   __syncthreads();
   uint16_t* dst = static_cast<uint16_t*>(a.nchw_dst) +
