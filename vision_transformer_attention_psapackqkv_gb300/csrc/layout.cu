@@ -17,6 +17,7 @@
 
 #include "attn.cuh"
 #include "layout.cuh"
+#include "ptx.cuh"
 
 namespace psa {
 
@@ -100,12 +101,15 @@ __global__ void __launch_bounds__(kThreads) rows_to_channels_kernel(TransposeArg
 // thread, transposed in registers with byte permutes): its warp reads or writes
 // the chunks (8g + i, c) of 8 c and 4 g per instruction without bank conflicts,
 // and in global memory the threads of one c cover whole position rows side by
-// side.  The channel-row side moves chunks along the NCHW rows, four per thread
-// in flight.
+// side.  The channel-row side moves chunks along the NCHW rows (up to eight per
+// thread in flight when loading them).
 constexpr int kVecTileN = 512;
 constexpr int kVecChunks = kVecTileN / 8;  // 16-byte chunks per channel row of the tile
 
 __device__ __forceinline__ int vec_chunk(int d, int c) { return d * kVecChunks + (c ^ ((d >> 3) & 7)); }
+// channel-row loads in flight per thread (a tile of 32 channels x 400 positions
+// is 6.25 per thread: one round trip instead of two)
+constexpr int kLoadsInFlight = 8;
 
 // Row j of the 8 x 8 transpose of 16-bit elements held as eight 16-byte vectors:
 // in[i] holds elements (i, 0..7) (two per 32-bit word, the lower index in the low
@@ -130,6 +134,10 @@ __device__ __forceinline__ P plane_ptr(const P (&p)[4], int s) {
 __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const TransposeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* tile = reinterpret_cast<uint4*>(smem_raw);  // KD x kVecChunks chunks
+  // launched with programmatic dependent launch: the next kernel may start its
+  // CTAs once every CTA here has begun; this one waits for the previous kernel
+  pdl_launch_dependents();
+  pdl_wait();
   const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
   const int unit = blockIdx.x / ntiles;
   const int s = unit % a.planes;
@@ -142,10 +150,10 @@ __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const
                         ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
                          (long long)s * a.KD) * a.N + n0;
   const int nload = a.KD * cvalid;
-  for (int i0 = threadIdx.x; i0 < nload; i0 += 4 * kThreads) {
-    uint4 v[4];
+  for (int i0 = threadIdx.x; i0 < nload; i0 += kLoadsInFlight * kThreads) {
+    uint4 v[kLoadsInFlight];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kLoadsInFlight; ++u) {
       const int idx = i0 + u * kThreads;
       if (idx < nload) {
         const int d = idx / cvalid, c = idx - d * cvalid;
@@ -153,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kLoadsInFlight; ++u) {
       const int idx = i0 + u * kThreads;
       if (idx < nload) {
         const int d = idx / cvalid, c = idx - d * cvalid;
@@ -182,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const
 __global__ void __launch_bounds__(kThreads, 4) rows_to_channels_vec_kernel(const TransposeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* tile = reinterpret_cast<uint4*>(smem_raw);
+  pdl_launch_dependents();  // (programmatic dependent launch, as above)
+  pdl_wait();
   const int ntiles = (a.N + kVecTileN - 1) / kVecTileN;
   const int unit = blockIdx.x / ntiles;
   const int s = unit % a.planes;
@@ -222,6 +232,8 @@ __global__ void __launch_bounds__(kThreads)
     strided_slab_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                              long long slabs, long long slab_vec, long long src_stride_vec,
                              long long dst_stride_vec) {
+  pdl_launch_dependents();  // (programmatic dependent launch)
+  pdl_wait();
   const long long total = slabs * slab_vec;
   for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < total;
        i += (long long)gridDim.x * kThreads) {
@@ -257,11 +269,10 @@ cudaError_t transpose(bool to_rows, const TransposeArgs& a, int B, int elem_byte
         to_rows ? (const void*)channels_to_rows_vec_kernel : (const void*)rows_to_channels_vec_kernel,
         128 * kVecTileN * 2);  // the largest tile (key_dim 128), set once per device
     if (attr != cudaSuccess) return attr;
-    if (to_rows)
-      channels_to_rows_vec_kernel<<<(unsigned)tiles, kThreads, smem, st>>>(a);
-    else
-      rows_to_channels_vec_kernel<<<(unsigned)tiles, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return to_rows ? launch_pdl(channels_to_rows_vec_kernel, dim3((unsigned)tiles), dim3(kThreads),
+                                smem, st, a)
+                   : launch_pdl(rows_to_channels_vec_kernel, dim3((unsigned)tiles), dim3(kThreads),
+                                smem, st, a);
   }
   return elem_bytes == 2 ? launch_transpose<uint16_t>(to_rows, a, B, st)
                          : launch_transpose<uint32_t>(to_rows, a, B, st);
@@ -330,9 +341,8 @@ cudaError_t launch_extract_v(const void* qkv, void* v, int B, int nh, int KD, in
   long long blocks = (total + kThreads - 1) / kThreads;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
-  strided_slab_copy_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(
-      src, static_cast<uint4*>(v), slabs, slab_vec, 2 * slab_vec, slab_vec);
-  return cudaGetLastError();
+  return launch_pdl(strided_slab_copy_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, src,
+                    static_cast<uint4*>(v), slabs, slab_vec, 2 * slab_vec, slab_vec);
 }
 
 }  // namespace psa
