@@ -556,13 +556,13 @@ __global__ void __launch_bounds__(896, 1)
       // channels 8s .. 8s+7 at positions 8g .. 8g+7 of the pass; the eight channel
       // slices meet in a scratch area of shared memory.
       static_assert(C::kRowWarps * 32 == C::CHUNK && DV == 64, "one thread per 8 x 8 block");
-      for (int c0 = 0; ok && c0 < N; c0 += C::CHUNK) {
+      for (int p0 = 0; ok && p0 < N; p0 += C::CHUNK) {
         const int t = threadIdx.x, g = t & 63, sl8 = t >> 6;
         float part[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) part[e] = 0.f;
-        if (c0 + 8 * g < N) {
-          const long long base = ((long long)out_row(bh) + 8 * sl8) * N + c0 + 8 * g;
+        if (p0 + 8 * g < N) {
+          const long long base = ((long long)out_row(bh) + 8 * sl8) * N + p0 + 8 * g;
           uint4 ov[8], dv[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(896, 1)
         float dsum = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) dsum += scratch[k * C::CHUNK + t];
-        hst[C::MAXN + c0 + t] = c0 + t < N ? -dsum : 0.f;
+        hst[C::MAXN + p0 + t] = p0 + t < N ? -dsum : 0.f;
         mbar_arrive(&b.dl_full);
         if (!mbar_wait(&b.dl_full, dlc & 1, abort)) {
           ok = false;
