@@ -554,6 +554,14 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
       const int q0 = qt * C::BM, q = q0 + r;
       const bool active = wq * 32 < N - q0, live = q < N;
       const int klast = i * nkv + nkv - 1;
+      // split rows: the row's (max, sum) go to the other half while the last P.V
+      // runs (the exchange area alternates with the tile parity)
+      float* ml = reinterpret_cast<float*>(smem + w * C::SL_BYTES + C::SL_ML) + (i & 1) * 512;
+      if (kSplit) {
+        ml[h * 256 + 2 * r] = m_run;
+        ml[h * 256 + 2 * r + 1] = l_run;
+        mbar_arrive(&b.ml_ready);
+      }
       if (!mbar_wait(&b.pv_done[klast & 1], (klast >> 1) & 1, abort)) return false;
       tc_fence_after();
       // NCHW: the staging area is free once the previous tile's stores have read it
@@ -562,10 +570,6 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
       if (kSplit) {
         // both halves' (max, sum) of the row, then this thread writes channels
         // [h * DV/2, (h + 1) * DV/2) of O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l
-        float* ml = reinterpret_cast<float*>(smem + w * C::SL_BYTES + C::SL_ML) + (i & 1) * 512;
-        ml[h * 256 + 2 * r] = m_run;
-        ml[h * 256 + 2 * r + 1] = l_run;
-        mbar_arrive(&b.ml_ready);
         if (!mbar_wait(&b.ml_ready, i & 1, abort)) return false;
         const float m0 = ml[2 * r], l0 = ml[2 * r + 1];
         const float m1 = ml[256 + 2 * r], l1 = ml[256 + 2 * r + 1];
