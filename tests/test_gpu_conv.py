@@ -36,6 +36,11 @@ def run_conv(ins):
     (1, 64, 64, 16, 16, False),    # no bias
     (2, 20, 48, 6, 6, True),       # cin % 8 != 0: CUDA cores
     (1, 64, 128, 7, 7, True),      # N = 49: CUDA cores
+    # enough tiles for two or more per CTA on 152 SMs: the weight-resident form
+    (20, 256, 512, 20, 20, True),  # tiles written by TMA stores (cin <= 256)
+    (76, 72, 200, 9, 16, True),    # the same with partial K, channel and position tiles
+    (10, 512, 1024, 20, 20, True), # 512 input channels: the threads' own stores
+    (152, 328, 136, 8, 10, False), # the same with partial tiles, no bias
 ])
 def test_qkv_conv(oracle, Bn, cin, cout, H, W, bias):
     ins = conv_inputs(Bn, cin, cout, H, W, seed=cin + cout + H, with_bias=bias)

@@ -154,8 +154,8 @@ bool map_nchw_store(CUtensorMap* m, void* base, long long rows, int N, int box_r
 
 // Tensor maps of the QKV convolution: w [cout, cin] (box {64, 128}) and x viewed as
 // 3-D (N, cin, B) (box {64, 64, 1}); positions and channels past the ends read as 0.
-bool map_conv(CUtensorMap* mw, CUtensorMap* mx, const void* w, const void* x, int B, int cin,
-              int cout, int N) {
+bool map_conv(CUtensorMap* mw, CUtensorMap* mx, CUtensorMap* mo, const void* w, const void* x,
+              void* out, int B, int cin, int cout, int N) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t wd[2] = {(cuuint64_t)cin, (cuuint64_t)cout};
@@ -170,9 +170,17 @@ bool map_conv(CUtensorMap* mw, CUtensorMap* mx, const void* w, const void* x, in
   cuuint64_t xs[2] = {(cuuint64_t)N * 2, (cuuint64_t)cin * N * 2};
   cuuint32_t xb[3] = {64, 64, 1};
   cuuint32_t e3[3] = {1, 1, 1};
-  return enc(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), xd, xs, xb, e3,
+  if (enc(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), xd, xs, xb, e3,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  // output tiles for TMA stores: 64 positions x 128 output channels of one batch item
+  cuuint64_t od[3] = {(cuuint64_t)N, (cuuint64_t)cout, (cuuint64_t)B};
+  cuuint64_t os[2] = {(cuuint64_t)N * 2, (cuuint64_t)cout * N * 2};
+  cuuint32_t ob[3] = {64, 128, 1};
+  return enc(mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, od, os, ob, e3,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 psa_status_t check_fa2(const void* const* ptrs, int nptr, int BH, int n_ctx, int head_dim,
@@ -229,9 +237,9 @@ psa_status_t psa_qkv_conv(const void* x, const void* w, const float* bias, void*
   a.bias = bias;
   a.out = static_cast<__nv_bfloat16*>(qkv);
   if (cin % 8 == 0 && N % 8 == 0) {
-    CUtensorMap mw, mx;
-    if (!map_conv(&mw, &mx, w, x, B, cin, cout, (int)N)) return PSA_ERR_CUDA;
-    return from_cuda(psa::launch_qkv_conv_tc(mw, mx, a, st));
+    CUtensorMap mw, mx, mo;
+    if (!map_conv(&mw, &mx, &mo, w, x, qkv, B, cin, cout, (int)N)) return PSA_ERR_CUDA;
+    return from_cuda(psa::launch_qkv_conv_tc(mw, mx, mo, a, st));
   }
   if (cout > 65535 || B > 65535) return PSA_ERR_UNSUPPORTED;
   return from_cuda(psa::launch_qkv_conv_simt(x, w, a, st));

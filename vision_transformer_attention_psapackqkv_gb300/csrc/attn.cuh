@@ -133,9 +133,10 @@ struct ConvArgs {
   __nv_bfloat16* out;
 };
 // Tensor cores: mW 2-D over w (box {64, 128}), mX 3-D over x (box {64, 64, 1}),
-// both with the 128-byte swizzle; needs cin % 8 == 0 and N % 8 == 0.
-cudaError_t launch_qkv_conv_tc(const CUtensorMap& mW, const CUtensorMap& mX, const ConvArgs& a,
-                               cudaStream_t st);
+// mOut 3-D over out (box {64, 128, 1}), all with the 128-byte swizzle; needs
+// cin % 8 == 0 and N % 8 == 0.
+cudaError_t launch_qkv_conv_tc(const CUtensorMap& mW, const CUtensorMap& mX,
+                               const CUtensorMap& mOut, const ConvArgs& a, cudaStream_t st);
 // CUDA cores, any shape.
 cudaError_t launch_qkv_conv_simt(const void* x, const void* w, const ConvArgs& a, cudaStream_t st);
 
