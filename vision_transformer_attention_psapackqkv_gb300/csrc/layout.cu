@@ -107,9 +107,8 @@ constexpr int kVecTileN = 512;
 constexpr int kVecChunks = kVecTileN / 8;  // 16-byte chunks per channel row of the tile
 
 __device__ __forceinline__ int vec_chunk(int d, int c) { return d * kVecChunks + (c ^ ((d >> 3) & 7)); }
-// channel-row loads in flight per thread (a tile of 32 channels x 400 positions
-// is 6.25 per thread: one round trip instead of two)
-constexpr int kLoadsInFlight = 8;
+constexpr int kWarps = kThreads / 32;
+static_assert(kVecChunks == 64, "two 16-byte chunks per lane cover a channel row of the tile");
 
 // Row j of the 8 x 8 transpose of 16-bit elements held as eight 16-byte vectors:
 // in[i] holds elements (i, 0..7) (two per 32-bit word, the lower index in the low
@@ -149,25 +148,27 @@ __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const
   const uint16_t* src = static_cast<const uint16_t*>(a.nchw_src) +
                         ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
                          (long long)s * a.KD) * a.N + n0;
-  const int nload = a.KD * cvalid;
-  for (int i0 = threadIdx.x; i0 < nload; i0 += kLoadsInFlight * kThreads) {
-    uint4 v[kLoadsInFlight];
+  // channel rows d = warp + kWarps i, 16-byte chunks c = lane + 32 h of each row
+  // (cvalid <= 64): a warp reads 512 contiguous bytes per instruction, eight loads
+  // in flight per thread, and no index needs a division
+  const int wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  for (int d0 = wid; d0 < a.KD; d0 += 4 * kWarps) {
+    uint4 v[4][2];
 #pragma unroll
-    for (int u = 0; u < kLoadsInFlight; ++u) {
-      const int idx = i0 + u * kThreads;
-      if (idx < nload) {
-        const int d = idx / cvalid, c = idx - d * cvalid;
-        v[u] = __ldg(reinterpret_cast<const uint4*>(src + (long long)d * a.N + 8 * c));
-      }
-    }
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int u = 0; u < kLoadsInFlight; ++u) {
-      const int idx = i0 + u * kThreads;
-      if (idx < nload) {
-        const int d = idx / cvalid, c = idx - d * cvalid;
-        tile[vec_chunk(d, c)] = v[u];
+      for (int h = 0; h < 2; ++h) {
+        const int d = d0 + i * kWarps, c = ln + 32 * h;
+        if (d < a.KD && c < cvalid)
+          v[i][h] = __ldg(reinterpret_cast<const uint4*>(src + (long long)d * a.N + 8 * c));
       }
-    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int d = d0 + i * kWarps, c = ln + 32 * h;
+        if (d < a.KD && c < cvalid) tile[vec_chunk(d, c)] = v[i][h];
+      }
   }
   __syncthreads();
   // one item = channels 8g .. 8g+7 x positions 8c .. 8c+7: eight chunk reads, a
@@ -177,8 +178,12 @@ __global__ void __launch_bounds__(kThreads, 4) channels_to_rows_vec_kernel(const
   uint4* dst = reinterpret_cast<uint4*>(plane_ptr(a.rows_dst, s)) +
                ((long long)bhd * a.N + n0) * dvec;
   const int nitems = dvec * cvalid;
+  // item idx -> (c, g) = (idx / dvec, idx % dvec); dvec = KD / 8 is a power of two
+  // for every power-of-two key_dim, where a shift replaces the division
+  const bool pow2 = (dvec & (dvec - 1)) == 0;
+  const int lg = 31 - __clz(dvec);
   for (int idx = threadIdx.x; idx < nitems; idx += kThreads) {
-    const int c = idx / dvec, g = idx - c * dvec;
+    const int c = pow2 ? idx >> lg : idx / dvec, g = idx - c * dvec;
     uint4 in[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) in[i] = tile[vec_chunk(8 * g + i, c)];
@@ -206,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 4) rows_to_channels_vec_kernel(const
   // one item = positions 8c .. 8c+7 x channels 8g .. 8g+7: eight position-row
   // reads (eight in flight), a register transpose, eight chunk writes
   const int nitems = dvec * cvalid;
+  const bool pow2 = (dvec & (dvec - 1)) == 0;  // (as in the other direction)
+  const int lg = 31 - __clz(dvec);
   for (int idx = threadIdx.x; idx < nitems; idx += kThreads) {
-    const int c = idx / dvec, g = idx - c * dvec;
+    const int c = pow2 ? idx >> lg : idx / dvec, g = idx - c * dvec;
     uint4 in[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) in[j] = __ldg(src + (long long)(8 * c + j) * dvec + g);
@@ -218,12 +225,15 @@ __global__ void __launch_bounds__(kThreads, 4) rows_to_channels_vec_kernel(const
   uint16_t* dst = static_cast<uint16_t*>(a.nchw_dst) +
                   ((long long)b * a.ch_per_batch + (long long)head * a.ch_per_head +
                    (long long)s * a.KD) * a.N + n0;
-  const int nstore = a.KD * cvalid;
-#pragma unroll 4
-  for (int idx = threadIdx.x; idx < nstore; idx += kThreads) {
-    const int d = idx / cvalid, c = idx - d * cvalid;
-    *reinterpret_cast<uint4*>(dst + (long long)d * a.N + 8 * c) = tile[vec_chunk(d, c)];
-  }
+  // channel rows d = warp + kWarps i, chunks c = lane + 32 h (as the loads of the
+  // other direction)
+  const int wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  for (int d = wid; d < a.KD; d += kWarps)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = ln + 32 * h;
+      if (c < cvalid) *reinterpret_cast<uint4*>(dst + (long long)d * a.N + 8 * c) = tile[vec_chunk(d, c)];
+    }
 }
 
 // Copies `slabs` contiguous slabs of slab_vec 16-byte vectors from src (slab
