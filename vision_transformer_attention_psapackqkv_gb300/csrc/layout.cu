@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) rows_to_channels_kernel(TransposeArg
 // thread, transposed in registers with byte permutes): its warp reads or writes
 // the chunks (8g + i, c) of 8 c and 4 g per instruction without bank conflicts,
 // and in global memory the threads of one c cover whole position rows side by
-// side.  The channel-row side moves chunks along the NCHW rows (up to eight per
-// thread in flight when loading them).
+// side.  The channel-row side moves chunks along the NCHW rows, a warp per row
+// and a lane per chunk (up to eight per thread in flight when loading them).
 constexpr int kVecTileN = 512;
 constexpr int kVecChunks = kVecTileN / 8;  // 16-byte chunks per channel row of the tile
 
