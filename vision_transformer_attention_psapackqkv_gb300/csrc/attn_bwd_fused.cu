@@ -657,8 +657,10 @@ __global__ void __launch_bounds__(896, 1)
               st_shared_v4(half + swizzled_offset(r, c0 / 8 + i, 128), dw[4 * i], dw[4 * i + 1],
                            dw[4 * i + 2], dw[4 * i + 3]);
           }
-          if (active) tmem_wait_st();
-          fence_proxy_async_smem();
+          if (active) {
+            tmem_wait_st();
+            fence_proxy_async_smem();  // (only active threads stored dS^T)
+          }
           tc_fence_before();
           mbar_arrive(&b.p_full[bb]);
         }

@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
           args.lse[(long long)bh * N + q] = lse;
       }
       if (kNCHW) {
-        fence_proxy_async_smem();
+        if (active) fence_proxy_async_smem();  // (only active warps wrote the staging tile)
         mbar_arrive(&b.out_full);
       }
       return true;
@@ -674,13 +674,13 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
           for (int c = 0; c < C::HC / 2; c += 16) tmem_store16_async(tP + c, s + c);
           tmem_wait_st();
           // O may only be rescaled once every earlier P.V has landed in it
-          if (__any_sync(0xffffffffu, alpha != 1.f) &&
-              !mbar_wait(&b.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort)) {
+          const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+          if (rescale && !mbar_wait(&b.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          if (rescale) {
 #pragma unroll 1
             for (int c = 0; c < DV; c += 32) {
               float o[32];
