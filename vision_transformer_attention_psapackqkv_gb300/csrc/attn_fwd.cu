@@ -411,6 +411,9 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
       constexpr uint64_t kStepV = kstep_ch_by_pos<kNCHW, DV>();
       const uint32_t idS_full = idesc_bf16_f32(128, C::BN, kNCHW, kNCHW);
       const uint32_t idPV = idesc_bf16_f32(128, DV, false, !kNCHW);
+      // query tile and V-slab row of each slot's current tile for the PsaExtractV
+      // stores, worked out once per tile (integer divisions off the per-step path)
+      int vqt[NWG], vrow0[NWG];
       auto issue_s = [&](int w, int i, int j) -> bool {
         SlotBars& b = bars[w];
         const int k = i * nkv + j;
@@ -437,12 +440,16 @@ __global__ void __launch_bounds__(128 * NWG * (kSplit ? 2 : 1) + 128, NWG == 1 ?
           // (already in shared memory for P.V) to the NCHW output with TMA; the
           // stage is released once the store has read it
           if (args.vres != nullptr) {
-            int bh, qt;
-            tile_coords(slot_tile(blockIdx.x * NWG + w, i, nslots), args.BH, nfull, bh, qt);
-            if ((j * C::BN) / C::BM == qt) {
+            if (j == 0) {
+              int bh, qt;
+              tile_coords(slot_tile(blockIdx.x * NWG + w, i, nslots), args.BH, nfull, bh, qt);
+              vqt[w] = qt;
+              vrow0[w] = (bh / args.nh) * args.vres_ch + (bh % args.nh) * DV;
+            }
+            if ((j * C::BN) / C::BM == vqt[w]) {
               const unsigned char* vt =
                   smem + w * C::SL_BYTES + C::SL_V + (k % C::STAGES) * C::V_BYTES;
-              const int vrow = (bh / args.nh) * args.vres_ch + (bh % args.nh) * DV;
+              const int vrow = vrow0[w];
 #pragma unroll
               for (int bx = 0; bx < C::BN / 64; ++bx)
                 tma_store_2d(&tmVres, vt + bx * (DV * 128), j * C::BN + 64 * bx, vrow);
